@@ -1,0 +1,252 @@
+/*
+ * kvq -- quantized paged KV cache for single-token decode (GB300, sm_103a).
+ *
+ * C ABI of libkvq.so.  Every argument is a plain pointer or size; device
+ * pointers are CUDA device memory owned by the caller.  The library never
+ * allocates or frees device memory, keeps no state between calls except a
+ * per-device error word (kvq_get_device_error) and a cached SM count, and
+ * enqueues all work asynchronously on the stream given (NULL = the legacy
+ * default stream).  Entry points are thread-safe.
+ *
+ * Errors: every check that can be made on the host (null pointers, sizes,
+ * unsupported shapes or formats, workspace too small, misalignment) returns
+ * a status before anything is launched.  A failed launch returns
+ * KVQ_ERR_CUDA.  Device-side data (slot ids, block ids) is range-checked in
+ * the kernels: an out-of-range id skips the access and sets a bit in the
+ * device error word instead of faulting.
+ *
+ * The operations follow the source pages:
+ *  - "vllm-int8-kv-cache-for-ampere-sm86" (project summary): INT8 KV cache
+ *    with per-layer scales, optional FP8-E4M3 for one of the two tensors;
+ *  - vLLM PR #4893 "Load FP8 kv-cache scaling factors from checkpoints"
+ *    (items 1-3, side note): --kv-cache-dtype fp8 / fp8_e4m3 / fp8_e5m2 with
+ *    a kv_scale, 1.0 when uncalibrated; FP8 decode runs in the paged-attention
+ *    kernel;
+ *  - vLLM issue #4025 "Support for 4-bit KV Cache in paged-attention op"
+ *    (section 'methods', items 1-3): scale/zero-point computation, int4
+ *    storage in write_to_paged_cache, paged attention taking k_scale,
+ *    k_zeropoint, v_scale, v_zeropoint;
+ *  - "KVarN : le backend natif pour la quantification du cache KV" (section
+ *    'Contexte Technique'): Hadamard rotation + variance normalisation +
+ *    asymmetric quantization, no calibration.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* kvq_stream_t;
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, misaligned buffer */
+  KVQ_ERR_UNSUPPORTED = 2,      /* valid but not implemented (head_dim, block_size, format) */
+  KVQ_ERR_WORKSPACE = 3,        /* workspace smaller than kvq_decode_workspace_size */
+  KVQ_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+} kvq_status;
+
+/* Stored code formats (the --kv-cache-dtype choices of PR #4893 item 1 plus
+ * the INT8 and INT4 caches of the INT8 summary and issue #4025). */
+typedef enum {
+  KVQ_FMT_INT8 = 1,       /* int8, symmetric, one fp32 scale per tensor          */
+  KVQ_FMT_FP8_E4M3 = 2,   /* OCP E4M3FN byte, one fp32 scale per tensor          */
+  KVQ_FMT_FP8_E5M2 = 3,   /* OCP E5M2 byte, one fp32 scale per tensor            */
+  KVQ_FMT_INT4_ASYM = 4,  /* 4-bit code, fp16 scale + zero point per token-head  */
+  KVQ_FMT_UINT8_ASYM = 5, /* 8-bit code, fp16 scale + zero point per token-head  */
+} kvq_format;
+
+/* KVarN pre-quantization (both tensors; asymmetric formats only): per
+ * (token, kv-head) row, divide by its fp16 standard deviation sigma, flip
+ * signs by d, apply the orthonormal Walsh-Hadamard transform; store sigma. */
+#define KVQ_FLAG_VARNORM_ROTATE 1u
+
+/*
+ * Description of one layer's paged cache (all device memory caller-owned).
+ *
+ * Code arrays (passed separately to the calls):
+ *   k_cache, v_cache: [num_blocks, block_size, num_kv_heads, row_bytes] bytes,
+ *   row_bytes = head_dim for 8-bit formats, head_dim/2 for INT4 (element 2i
+ *   in the low nibble of byte i, element 2i+1 in the high nibble); int8
+ *   codes are two's complement.  16-byte aligned.
+ * Metadata (asymmetric formats only, else NULL):
+ *   k_meta, v_meta: fp16 [num_blocks, num_kv_heads, F, block_size] with
+ *   F = 2 fields (scale, zero point) or 3 (scale, zero point, sigma) with
+ *   KVQ_FLAG_VARNORM_ROTATE.  16-byte aligned.
+ *   Dequantization: x = (code * scale + zero_point) [* sigma, then the
+ *   inverse rotation].
+ * Per-tensor scales (symmetric formats): x = code_value * k_scale (v_scale).
+ * signs: device int8 [head_dim] of +1 / -1 (the rotation's diagonal), or
+ *   NULL for all +1; read only with KVQ_FLAG_VARNORM_ROTATE.
+ */
+typedef struct {
+  int32_t k_fmt;        /* kvq_format */
+  int32_t v_fmt;        /* kvq_format */
+  int32_t num_kv_heads; /* >= 1 */
+  int32_t head_dim;     /* 64 or 128 */
+  int32_t block_size;   /* 16 or 32 tokens per block */
+  int32_t num_blocks;   /* >= 1 */
+  uint32_t flags;       /* KVQ_FLAG_* */
+  float k_scale;        /* symmetric K formats: > 0 (1.0 = uncalibrated fp8) */
+  float v_scale;        /* symmetric V formats: > 0 */
+  void* k_meta;
+  void* v_meta;
+  const int8_t* signs;
+} kvq_cache_desc;
+
+/*
+ * kvq_write_cache -- quantize bf16 keys/values and scatter them into the
+ * paged cache ("write_to_paged_cache" of issue #4025, 'methods' items 1-2;
+ * the INT8 / FP8 caches of the INT8 summary and PR #4893).
+ *
+ * key, value: device bf16 [num_tokens, num_kv_heads, head_dim]; heads and
+ *   elements contiguous, consecutive tokens `key_stride` / `value_stride`
+ *   elements apart (>= num_kv_heads*head_dim, multiple of 8); 16-byte aligned.
+ * slot_mapping: device int64 [num_tokens]; token t is written at
+ *   block = slot / block_size, offset = slot % block_size; slot < 0 skips the
+ *   token; a slot past the cache sets KVQ_DEVERR_SLOT_RANGE and is skipped.
+ *   Two tokens with the same slot: which one lands is unspecified.
+ * Codes (fixed float32 arithmetic, IEEE round-to-nearest, no contraction):
+ *   INT8:  clamp(rint(x * inv), -128, 127), inv = 1.0f / scale
+ *   FP8:   E4M3 / E5M2 of (x * inv), round to nearest even, saturating to
+ *          the largest finite magnitude
+ *   ASYM:  s = fp16((max - min) / L) (1 if it is 0), z = fp16(min),
+ *          code = clamp(rint((x - z) * (1.0f / s)), 0, L), L = 15 or 255.
+ *   With KVQ_FLAG_VARNORM_ROTATE the ASYM step runs on the normalised,
+ *   rotated row (see kvq_hadamard for the transform's definition).
+ * Slots that are not written are left untouched.  num_tokens == 0 is a no-op.
+ */
+kvq_status kvq_write_cache(const kvq_cache_desc* cache, void* k_cache, void* v_cache,
+                           const void* key, const void* value, int64_t key_stride,
+                           int64_t value_stride, const int64_t* slot_mapping,
+                           int64_t num_tokens, kvq_stream_t stream);
+
+/*
+ * kvq_decode_workspace_size -- bytes of device workspace kvq_paged_decode
+ * needs for these sizes (0 when one context partition suffices).  Depends on
+ * the device's SM count (current device).
+ */
+kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t max_context_len,
+                                     size_t* bytes);
+
+/*
+ * kvq_paged_decode -- one new query token per sequence attends to its paged,
+ * quantized context (issue #4025 'methods' item 3; PR #4893 side note).
+ *
+ * query: device bf16 [num_seqs, num_q_heads, head_dim], contiguous.
+ * out:   device bf16 [num_seqs, num_q_heads, head_dim], contiguous.
+ *   q-head h reads kv-head h / (num_q_heads / num_kv_heads); the ratio must be
+ *   an integer <= 8.
+ * block_table: device int32 [num_seqs, max_blocks_per_seq]; entries past
+ *   ceil(context_len / block_size) are never read.
+ * context_lens: device int32 [num_seqs], each in [0, max_context_len] (a length
+ *   outside is clamped into it and sets KVQ_DEVERR_CONTEXT_RANGE).
+ *   context_len 0 gives out = 0.
+ * sm_scale: logits are sm_scale * <q, k>.
+ * workspace: device memory of >= kvq_decode_workspace_size(...) bytes
+ *   (may be NULL when that size is 0), 16-byte aligned, contents ignored.
+ * out[s, h] = sum_t softmax_t(sm_scale <q, k_t>) v_t over the dequantized
+ *   cache, computed with fp32 softmax and fp32 accumulation (keys and values
+ *   enter the tensor cores as exact fp16 code values; the query is rounded to
+ *   fp16, which is exact for bf16 values of magnitude 2^-14 .. 65504).
+ */
+kvq_status kvq_paged_decode(const kvq_cache_desc* cache, const void* k_cache,
+                            const void* v_cache, void* out, const void* query,
+                            int32_t num_seqs, int32_t num_q_heads, const int32_t* block_table,
+                            int32_t max_blocks_per_seq, const int32_t* context_lens,
+                            int32_t max_context_len, float sm_scale, void* workspace,
+                            size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * kvq_paged_decode_ex -- kvq_paged_decode with an explicit context
+ * partition size (tokens per split-K partition, a multiple of 64; 0 = the
+ * automatic choice).  The workspace must hold
+ * kvq_decode_workspace_size_ex(...) bytes for the same partition size.
+ */
+kvq_status kvq_decode_workspace_size_ex(const kvq_cache_desc* cache, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t max_context_len,
+                                        int32_t partition_tokens, size_t* bytes);
+kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
+                               const void* v_cache, void* out, const void* query,
+                               int32_t num_seqs, int32_t num_q_heads,
+                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t max_context_len,
+                               float sm_scale, int32_t partition_tokens, void* workspace,
+                               size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * The two launches of kvq_paged_decode_ex, callable separately with the same
+ * arguments (e.g. to time them, or to run the combine later on the stream):
+ * kvq_paged_decode_partitions runs the per-partition attention (and, when one
+ * partition covers every sequence, writes `out` itself); kvq_paged_decode_combine
+ * merges the partitions into `out` (a no-op with one partition).  Calling
+ * partitions then combine on one stream equals one kvq_paged_decode_ex call.
+ */
+kvq_status kvq_paged_decode_partitions(const kvq_cache_desc* cache, const void* k_cache,
+                                       const void* v_cache, void* out, const void* query,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       const int32_t* block_table, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t max_context_len,
+                                       float sm_scale, int32_t partition_tokens, void* workspace,
+                                       size_t workspace_bytes, kvq_stream_t stream);
+kvq_status kvq_paged_decode_combine(const kvq_cache_desc* cache, const void* k_cache,
+                                    const void* v_cache, void* out, const void* query,
+                                    int32_t num_seqs, int32_t num_q_heads,
+                                    const int32_t* block_table, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t max_context_len,
+                                    float sm_scale, int32_t partition_tokens, void* workspace,
+                                    size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * kvq_hadamard -- in-place orthonormal Walsh-Hadamard rotation of `rows`
+ * rows of `head_dim` elements (KVarN article, 'Contexte Technique').
+ *   forward (inverse = 0): x <- cR * H (d . x)
+ *   inverse (inverse = 1): x <- d . (cR * H x)
+ * H is the natural-order (Sylvester) Hadamard matrix, d = signs (NULL: all
+ * +1), cR = float(1/sqrt(head_dim)).  H x is computed in float32 by the
+ * butterfly stages h = 1, 2, 4, ..., head_dim/2 in that order, each pair
+ * (i, i+h), i & h == 0, becoming (a + b, a - b).  dtype: 0 = float32,
+ * 1 = bfloat16 (computed in float32, rounded to nearest even on store).
+ * x: device, contiguous rows, 16-byte aligned.  head_dim: 64, 128 or 256.
+ */
+kvq_status kvq_hadamard(void* x, int32_t dtype, int64_t rows, int32_t head_dim,
+                        const int8_t* signs, int32_t inverse, kvq_stream_t stream);
+
+/*
+ * kvq_calibrate_scale -- per-tensor scale = absmax(x) / qmax in float32
+ * (1.0 when x is all zero): the per-layer scaling values of the INT8
+ * summary (qmax 127) and the E4M3 kv_scale (qmax 448).
+ * x: device bf16 [n], finite values; scale_out: device float, overwritten.
+ */
+kvq_status kvq_calibrate_scale(const void* x, int64_t n, float qmax, float* scale_out,
+                               kvq_stream_t stream);
+
+/* Device error word bits. */
+#define KVQ_DEVERR_SLOT_RANGE 1u  /* a slot id past num_blocks*block_size */
+#define KVQ_DEVERR_BLOCK_RANGE 2u /* a block-table entry outside [0, num_blocks) */
+#define KVQ_DEVERR_CONTEXT_RANGE 4u /* a context length outside [0, max_context_len] */
+
+/*
+ * kvq_get_device_error -- synchronizes `stream`, then reads and clears the
+ * current device's error word (OR of KVQ_DEVERR_* bits set since the last
+ * read) into *bits.
+ */
+kvq_status kvq_get_device_error(kvq_stream_t stream, uint32_t* bits);
+
+/* Static string for a status code. */
+const char* kvq_status_string(kvq_status status);
+
+/* Library version, e.g. "kvq 0.1.0 sm_103a". */
+const char* kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

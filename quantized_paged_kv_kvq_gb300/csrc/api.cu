@@ -1,0 +1,343 @@
+// C ABI of libkvq.so: host-side argument validation and the stream-ordered
+// launcher (kernel variant and grid from format, head_dim, GQA ratio and
+// context length).  No allocation, no per-call state.
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "../../include/kvq.h"
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+using namespace kvq;
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_fmt(int f) { return f >= KVQ_FMT_INT8 && f <= KVQ_FMT_UINT8_ASYM; }
+
+bool pairing_ok(int kf, int vf, bool kvarn) {
+  const bool ak = is_asym(kf), av = is_asym(vf);
+  if (kvarn) return ak && av;
+  return ak == av;
+}
+
+// Checks shared by write and decode on the cache description.
+kvq_status check_cache(const kvq_cache_desc* c) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!valid_fmt(c->k_fmt) || !valid_fmt(c->v_fmt)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->num_kv_heads < 1 || c->num_blocks < 1 || c->block_size < 1 || c->head_dim < 1)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->flags & ~KVQ_FLAG_VARNORM_ROTATE) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (c->block_size != 16 && c->block_size != 32) return KVQ_ERR_UNSUPPORTED;
+  const bool kvarn = (c->flags & KVQ_FLAG_VARNORM_ROTATE) != 0;
+  if (!pairing_ok(c->k_fmt, c->v_fmt, kvarn)) return KVQ_ERR_UNSUPPORTED;
+  if (!is_asym(c->k_fmt) && !(c->k_scale > 0.0f && isfinite(c->k_scale)))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!is_asym(c->v_fmt) && !(c->v_scale > 0.0f && isfinite(c->v_scale)))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (is_asym(c->k_fmt) && (c->k_meta == nullptr || !aligned(c->k_meta, 16)))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (is_asym(c->v_fmt) && (c->v_meta == nullptr || !aligned(c->v_meta, 16)))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (kvarn && c->signs != nullptr && !aligned(c->signs, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+  return KVQ_OK;
+}
+
+float rotation_scale(int d) { return static_cast<float>(1.0 / sqrt(static_cast<double>(d))); }
+
+// SM count of the current device, cached per device.
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  int v = (dev >= 0 && dev < 64) ? cache[dev].load() : 0;
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cache[dev].store(v);
+  return v;
+}
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Tokens per context partition: aim at a few waves of resident CTAs while
+// keeping partitions long enough that the split-K workspace stays small.
+int auto_partition(int num_seqs, int hkv, int max_ctx, int sms) {
+  if (max_ctx <= 0) return 64;
+  const long long units = static_cast<long long>(num_seqs) * hkv;
+  const long long target = static_cast<long long>(sms > 0 ? sms : 152) * 3 * 4;
+  long long p = (static_cast<long long>(max_ctx) * units + target - 1) / target;
+  p = ((p + 63) / 64) * 64;
+  if (p < 256) p = 256;
+  if (p > kMaxPartition) p = kMaxPartition;
+  const long long whole = ((max_ctx + 63) / 64) * 64;
+  if (p >= whole && whole <= kMaxPartition) p = whole;
+  return static_cast<int>(p);
+}
+
+size_t workspace_bytes_for(int num_seqs, int hq, int d, int np) {
+  if (np <= 1) return 0;
+  const size_t rows = static_cast<size_t>(num_seqs) * hq * np;
+  const size_t acc = rows * d * sizeof(float);
+  return acc + rows * 2 * sizeof(float);
+}
+
+kvq_status decode_shape(const kvq_cache_desc* c, int32_t num_seqs, int32_t num_q_heads,
+                        int32_t max_context_len, int32_t partition_tokens, int* P, int* NP) {
+  kvq_status st = check_cache(c);
+  if (st != KVQ_OK) return st;
+  if (num_seqs < 0 || num_q_heads < 1 || max_context_len < 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_q_heads % c->num_kv_heads) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_q_heads / c->num_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;
+  if (partition_tokens < 0 || partition_tokens % 64 || partition_tokens > kMaxPartition)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  int p = partition_tokens;
+  if (p == 0) {
+    const int sms = sm_count();
+    if (sms <= 0) return KVQ_ERR_CUDA;
+    p = auto_partition(num_seqs, c->num_kv_heads, max_context_len, sms);
+  }
+  const int np = max_context_len > 0 ? ceil_div(max_context_len, p) : 1;
+  if (np > 65535 || num_seqs > 65535) return KVQ_ERR_UNSUPPORTED;
+  *P = p;
+  *NP = np;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_INVALID_ARGUMENT: return "KVQ_ERR_INVALID_ARGUMENT";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED";
+    case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA";
+  }
+  return "KVQ_ERR_UNKNOWN";
+}
+
+const char* kvq_version(void) { return "kvq 0.1.0 sm_103a"; }
+
+kvq_status kvq_write_cache(const kvq_cache_desc* cache, void* k_cache, void* v_cache,
+                           const void* key, const void* value, int64_t key_stride,
+                           int64_t value_stride, const int64_t* slot_mapping, int64_t num_tokens,
+                           kvq_stream_t stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (num_tokens < 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return KVQ_OK;
+  if (!k_cache || !v_cache || !key || !value || !slot_mapping) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(key, 16) || !aligned(value, 16) ||
+      !aligned(slot_mapping, 8))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  const int64_t row = static_cast<int64_t>(cache->num_kv_heads) * cache->head_dim;
+  if (key_stride < row || value_stride < row || key_stride % 8 || value_stride % 8)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_tokens > (1LL << 31) * 8) return KVQ_ERR_UNSUPPORTED;
+  const bool kvarn = (cache->flags & KVQ_FLAG_VARNORM_ROTATE) != 0;
+  WriteArgs a;
+  a.key = static_cast<const uint16_t*>(key);
+  a.value = static_cast<const uint16_t*>(value);
+  a.key_stride = key_stride;
+  a.value_stride = value_stride;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.k_cache = static_cast<uint8_t*>(k_cache);
+  a.v_cache = static_cast<uint8_t*>(v_cache);
+  a.k_meta = static_cast<__half*>(cache->k_meta);
+  a.v_meta = static_cast<__half*>(cache->v_meta);
+  a.num_kv_heads = cache->num_kv_heads;
+  a.block_size = cache->block_size;
+  a.num_blocks = cache->num_blocks;
+  // inv = 1/scale, one IEEE float32 division on the host
+  volatile float one = 1.0f;
+  a.k_inv = is_asym(cache->k_fmt) ? 1.0f : one / cache->k_scale;
+  a.v_inv = is_asym(cache->v_fmt) ? 1.0f : one / cache->v_scale;
+  a.signs = cache->signs;
+  a.cR = rotation_scale(cache->head_dim);
+  const cudaError_t e =
+      launch_write(a, cache->head_dim, cache->k_fmt, cache->v_fmt, kvarn, stream);
+  if (e == cudaErrorNotSupported) return KVQ_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_decode_workspace_size_ex(const kvq_cache_desc* cache, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t max_context_len,
+                                        int32_t partition_tokens, size_t* bytes) {
+  if (bytes == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  int P = 0, NP = 0;
+  kvq_status st =
+      decode_shape(cache, num_seqs, num_q_heads, max_context_len, partition_tokens, &P, &NP);
+  if (st != KVQ_OK) return st;
+  *bytes = workspace_bytes_for(num_seqs, num_q_heads, cache->head_dim, NP);
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t max_context_len,
+                                     size_t* bytes) {
+  return kvq_decode_workspace_size_ex(cache, num_seqs, num_q_heads, max_context_len, 0, bytes);
+}
+
+namespace {
+
+kvq_status paged_decode_impl(const kvq_cache_desc* cache, const void* k_cache, const void* v_cache,
+                             void* out, const void* query, int32_t num_seqs, int32_t num_q_heads,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t max_context_len, float sm_scale,
+                             int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                             kvq_stream_t stream, int phase) {
+  int P = 0, NP = 0;
+  kvq_status st =
+      decode_shape(cache, num_seqs, num_q_heads, max_context_len, partition_tokens, &P, &NP);
+  if (st != KVQ_OK) return st;
+  if (num_seqs == 0) return KVQ_OK;
+  if (!k_cache || !v_cache || !out || !query || !block_table || !context_lens)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 2) || !aligned(query, 2) ||
+      !aligned(block_table, 4) || !aligned(context_lens, 4))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (max_blocks_per_seq < ceil_div(max_context_len, cache->block_size) || max_blocks_per_seq < 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!isfinite(sm_scale)) return KVQ_ERR_INVALID_ARGUMENT;
+  const size_t need = workspace_bytes_for(num_seqs, num_q_heads, cache->head_dim, NP);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KVQ_ERR_WORKSPACE;
+  if (need > 0 && !aligned(workspace, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+  const bool kvarn = (cache->flags & KVQ_FLAG_VARNORM_ROTATE) != 0;
+  DecodeArgs a;
+  a.k_cache = static_cast<const uint8_t*>(k_cache);
+  a.v_cache = static_cast<const uint8_t*>(v_cache);
+  a.k_meta = static_cast<const __half*>(cache->k_meta);
+  a.v_meta = static_cast<const __half*>(cache->v_meta);
+  a.query = static_cast<const uint16_t*>(query);
+  a.out = static_cast<uint16_t*>(out);
+  a.block_table = block_table;
+  a.context_lens = context_lens;
+  a.signs = cache->signs;
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * NP;
+  a.ws_acc = need ? static_cast<float*>(workspace) : nullptr;
+  a.ws_ml = need ? static_cast<float*>(workspace) + rows * cache->head_dim : nullptr;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.gqa = num_q_heads / cache->num_kv_heads;
+  a.block_size = cache->block_size;
+  a.num_blocks = cache->num_blocks;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_context_len = max_context_len;
+  a.partition_tokens = P;
+  a.num_partitions = NP;
+  a.qk_scale = sm_scale * kLog2e * (is_asym(cache->k_fmt) ? 1.0f : cache->k_scale);
+  a.v_scale = is_asym(cache->v_fmt) ? 1.0f : cache->v_scale;
+  a.cR = rotation_scale(cache->head_dim);
+  a.phase = phase;
+  cudaError_t e;
+  const int kf = cache->k_fmt, vf = cache->v_fmt;
+  if (is_asym(kf)) {
+    e = cache->head_dim == 64 ? launch_decode_d64_asym(a, kf, vf, kvarn, stream)
+                              : launch_decode_d128_asym(a, kf, vf, kvarn, stream);
+  } else {
+    e = cache->head_dim == 64 ? launch_decode_d64_sym(a, kf, vf, stream)
+                              : launch_decode_d128_sym(a, kf, vf, stream);
+  }
+  if (e == cudaErrorNotSupported) return KVQ_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace
+
+kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
+                               const void* v_cache, void* out, const void* query,
+                               int32_t num_seqs, int32_t num_q_heads, const int32_t* block_table,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t max_context_len, float sm_scale, int32_t partition_tokens,
+                               void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+  return paged_decode_impl(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
+                           max_blocks_per_seq, context_lens, max_context_len, sm_scale,
+                           partition_tokens, workspace, workspace_bytes, stream, 3);
+}
+
+kvq_status kvq_paged_decode_partitions(const kvq_cache_desc* cache, const void* k_cache,
+                                       const void* v_cache, void* out, const void* query,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       const int32_t* block_table, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t max_context_len,
+                                       float sm_scale, int32_t partition_tokens, void* workspace,
+                                       size_t workspace_bytes, kvq_stream_t stream) {
+  return paged_decode_impl(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
+                           max_blocks_per_seq, context_lens, max_context_len, sm_scale,
+                           partition_tokens, workspace, workspace_bytes, stream, 1);
+}
+
+kvq_status kvq_paged_decode_combine(const kvq_cache_desc* cache, const void* k_cache,
+                                    const void* v_cache, void* out, const void* query,
+                                    int32_t num_seqs, int32_t num_q_heads,
+                                    const int32_t* block_table, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t max_context_len,
+                                    float sm_scale, int32_t partition_tokens, void* workspace,
+                                    size_t workspace_bytes, kvq_stream_t stream) {
+  return paged_decode_impl(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
+                           max_blocks_per_seq, context_lens, max_context_len, sm_scale,
+                           partition_tokens, workspace, workspace_bytes, stream, 2);
+}
+
+kvq_status kvq_paged_decode(const kvq_cache_desc* cache, const void* k_cache,
+                            const void* v_cache, void* out, const void* query, int32_t num_seqs,
+                            int32_t num_q_heads, const int32_t* block_table,
+                            int32_t max_blocks_per_seq, const int32_t* context_lens,
+                            int32_t max_context_len, float sm_scale, void* workspace,
+                            size_t workspace_bytes, kvq_stream_t stream) {
+  return kvq_paged_decode_ex(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads,
+                             block_table, max_blocks_per_seq, context_lens, max_context_len,
+                             sm_scale, 0, workspace, workspace_bytes, stream);
+}
+
+kvq_status kvq_hadamard(void* x, int32_t dtype, int64_t rows, int32_t head_dim,
+                        const int8_t* signs, int32_t inverse, kvq_stream_t stream) {
+  if (rows < 0 || (dtype != 0 && dtype != 1) || (inverse != 0 && inverse != 1))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (rows == 0) return KVQ_OK;
+  if (x == nullptr || !aligned(x, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (signs != nullptr && !aligned(signs, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+  const cudaError_t e =
+      launch_hadamard(x, dtype, rows, head_dim, signs, inverse, rotation_scale(head_dim), stream);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_calibrate_scale(const void* x, int64_t n, float qmax, float* scale_out,
+                               kvq_stream_t stream) {
+  if (n < 0 || !(qmax > 0.0f && isfinite(qmax)) || scale_out == nullptr ||
+      !aligned(scale_out, 4))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (n > 0 && (x == nullptr || !aligned(x, 16))) return KVQ_ERR_INVALID_ARGUMENT;
+  const int sms = sm_count();
+  if (sms <= 0) return KVQ_ERR_CUDA;
+  const cudaError_t e =
+      launch_calibrate(static_cast<const uint16_t*>(x), n, qmax, scale_out, stream, sms);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_get_device_error(kvq_stream_t stream, uint32_t* bits) {
+  if (bits == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KVQ_ERR_CUDA;
+  unsigned v = 0;
+  cudaError_t (*take[])(unsigned*) = {take_error_bits_write, take_error_bits_decode_d64_sym,
+                                      take_error_bits_decode_d128_sym,
+                                      take_error_bits_decode_d64_asym,
+                                      take_error_bits_decode_d128_asym};
+  for (auto f : take)
+    if (f(&v) != cudaSuccess) return KVQ_ERR_CUDA;
+  *bits = v;
+  return KVQ_OK;
+}
+
+}  // extern "C"

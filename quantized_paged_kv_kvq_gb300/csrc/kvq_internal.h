@@ -1,0 +1,85 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+// Longest split-K context partition (tokens); bounds the block-id staging area.
+constexpr int kMaxPartition = 8192;
+
+struct WriteArgs {
+  const uint16_t* key;    // bf16 bits
+  const uint16_t* value;  // bf16 bits
+  int64_t key_stride;     // elements between tokens
+  int64_t value_stride;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  uint8_t* k_cache;
+  uint8_t* v_cache;
+  __half* k_meta;
+  __half* v_meta;
+  int num_kv_heads;
+  int block_size;
+  int num_blocks;
+  float k_inv;  // 1/k_scale (symmetric formats)
+  float v_inv;
+  const int8_t* signs;
+  float cR;  // float(1/sqrt(head_dim))
+};
+
+struct DecodeArgs {
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const __half* k_meta;
+  const __half* v_meta;
+  const uint16_t* query;  // bf16 [S, Hq, D]
+  uint16_t* out;          // bf16 [S, Hq, D]
+  const int32_t* block_table;
+  const int32_t* context_lens;
+  const int8_t* signs;
+  float* ws_acc;  // [S, Hq, NP, D]
+  float* ws_ml;   // [S, Hq, NP, 2]
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int gqa;
+  int block_size;
+  int num_blocks;
+  int max_blocks_per_seq;
+  int max_context_len;
+  int partition_tokens;  // P, multiple of 64
+  int num_partitions;    // NP
+  float qk_scale;        // sm_scale * log2(e) [* k_scale for symmetric K]
+  float v_scale;         // symmetric V: multiplies the output
+  float cR;
+  int phase;  // bit 0: partition kernel, bit 1: log-sum-exp combine
+};
+
+cudaError_t launch_write(const WriteArgs& a, int head_dim, int kf, int vf, bool kvarn,
+                         cudaStream_t st);
+bool write_supported(int kf, int vf, bool kvarn);
+
+cudaError_t launch_decode_d64_sym(const DecodeArgs& a, int kf, int vf, cudaStream_t st);
+cudaError_t launch_decode_d128_sym(const DecodeArgs& a, int kf, int vf, cudaStream_t st);
+cudaError_t launch_decode_d64_asym(const DecodeArgs& a, int kf, int vf, bool kvarn,
+                                   cudaStream_t st);
+cudaError_t launch_decode_d128_asym(const DecodeArgs& a, int kf, int vf, bool kvarn,
+                                    cudaStream_t st);
+
+// read-and-clear of each translation unit's device error word
+cudaError_t take_error_bits_write(unsigned* bits);
+cudaError_t take_error_bits_decode_d64_sym(unsigned* bits);
+cudaError_t take_error_bits_decode_d128_sym(unsigned* bits);
+cudaError_t take_error_bits_decode_d64_asym(unsigned* bits);
+cudaError_t take_error_bits_decode_d128_asym(unsigned* bits);
+
+cudaError_t launch_hadamard(void* x, int dtype, int64_t rows, int head_dim, const int8_t* signs,
+                            int inverse, float cR, cudaStream_t st);
+
+cudaError_t launch_calibrate(const uint16_t* x, int64_t n, float qmax, float* scale,
+                             cudaStream_t st, int num_sms);
+
+}  // namespace kvq

@@ -1,0 +1,313 @@
+// Quantize-and-scatter into the paged cache (write_to_paged_cache), plus the
+// per-tensor scale calibration.
+//
+// vLLM issue #4025 'Support for 4-bit KV Cache in paged-attention op',
+// section 'methods', items 1-2 (scale / zero point, int4 storage in the
+// paged-cache write); the INT8 cache with per-layer scales of the
+// "vllm-int8-kv-cache-for-ampere-sm86" summary; FP8 e4m3 / e5m2 with a
+// kv_scale from vLLM PR #4893 (item 1); the KVarN article's variance
+// normalisation + Hadamard rotation before asymmetric codes ('Contexte
+// Technique').
+//
+// Mapping: one warp per token.  A row (token, kv-head) of D bf16 values is
+// held by D/8 consecutive lanes, 8 consecutive elements (16 bytes) each, so
+// a warp covers 256/D rows per 16-byte load and every load and store is
+// fully coalesced.  Per-row reductions (min / max / sums) are xor-butterflies
+// inside the lane group.  HBM-bound: 2*D*2 bytes read and D or D/2 bytes
+// (+ meta) written per row.
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+KVQ_ERROR_ACCESSOR(take_error_bits_write)
+
+namespace {
+
+constexpr int kWriteWarps = 8;
+
+template <int D>
+struct RowGeom {
+  static constexpr int LPR = D / 8;     // lanes per row
+  static constexpr int RPI = 32 / LPR;  // rows per warp-wide 16-byte load
+};
+
+__device__ __forceinline__ void unpack8(const uint4& r, float (&x)[8]) {
+  x[0] = bf16_lo(r.x); x[1] = bf16_hi(r.x);
+  x[2] = bf16_lo(r.y); x[3] = bf16_hi(r.y);
+  x[4] = bf16_lo(r.z); x[5] = bf16_hi(r.z);
+  x[6] = bf16_lo(r.w); x[7] = bf16_hi(r.w);
+}
+
+// Fixed-order float32 sum of a row: 8 values per lane left to right, then
+// lane groups combined with xor offsets LPR/2, ..., 1.
+template <int LPR>
+__device__ __forceinline__ float tree_sum8(const float (&x)[8]) {
+  float s = x[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) s = __fadd_rn(s, x[i]);
+#pragma unroll
+  for (int o = LPR / 2; o >= 1; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+  return s;
+}
+
+// KVarN pre-quantization of one row, in place: x <- cR * H (d . x / sigma16).
+template <int D>
+__device__ __forceinline__ __half varnorm_rotate(float (&x)[8], int sub, uint32_t sign_bits,
+                                                 float cR) {
+  constexpr int LPR = RowGeom<D>::LPR;
+  const float inv_d = 1.0f / D;  // exact (power of two)
+  const float mean = __fmul_rn(tree_sum8<LPR>(x), inv_d);
+  float sq[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float dv = __fsub_rn(x[i], mean);
+    sq[i] = __fmul_rn(dv, dv);
+  }
+  const float var = __fmul_rn(tree_sum8<LPR>(sq), inv_d);
+  __half s16 = __float2half_rn(__fsqrt_rn(var));
+  if (__half2float(s16) == 0.0f) s16 = __float2half_rn(1.0f);
+  const float inv_sigma = __frcp_rn(__half2float(s16));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float y = __fmul_rn(x[i], inv_sigma);
+    x[i] = ((sign_bits >> i) & 1u) ? -y : y;
+  }
+  fwht_lanes<8, LPR>(x, sub);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], cR);
+  return s16;
+}
+
+// Quantize one row held by the lane group and store codes (+ meta).
+template <int D, int F, bool KVARN>
+__device__ __forceinline__ void quantize_store(float (&x)[8], bool active, int h, int sub,
+                                               size_t row, uint8_t* __restrict__ cache,
+                                               __half* __restrict__ meta, float inv, int64_t blk,
+                                               int off, int Hkv, int bs, uint32_t sign_bits,
+                                               float cR) {
+  constexpr int LPR = RowGeom<D>::LPR;
+  if constexpr (F == INT8) {
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int c = __float2int_rn(__fmul_rn(x[i], inv));
+      c = max(-128, min(127, c));
+      w[i >> 2] |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * (i & 3));
+    }
+    if (active) *reinterpret_cast<uint2*>(cache + row * D + sub * 8) = make_uint2(w[0], w[1]);
+  } else if constexpr (F == E4M3 || F == E5M2) {
+    uint32_t w[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t lo = f32x2_to_fp8x2<F>(__fmul_rn(x[4 * j], inv), __fmul_rn(x[4 * j + 1], inv));
+      const uint32_t hi =
+          f32x2_to_fp8x2<F>(__fmul_rn(x[4 * j + 2], inv), __fmul_rn(x[4 * j + 3], inv));
+      w[j] = lo | (hi << 16);
+    }
+    if (active) *reinterpret_cast<uint2*>(cache + row * D + sub * 8) = make_uint2(w[0], w[1]);
+  } else {
+    static_assert(is_asym(F), "format");
+    __half sig16 = __float2half_rn(1.0f);
+    if constexpr (KVARN) sig16 = varnorm_rotate<D>(x, sub, sign_bits, cR);
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      mn = fminf(mn, x[i]);
+      mx = fmaxf(mx, x[i]);
+    }
+#pragma unroll
+    for (int o = LPR / 2; o >= 1; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    constexpr int L = asym_levels(F);
+    __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(L)));
+    if (__half2float(s16) == 0.0f) s16 = __float2half_rn(1.0f);
+    const __half z16 = __float2half_rn(mn);
+    const float zf = __half2float(z16);
+    const float inv_s = __frcp_rn(__half2float(s16));
+    int c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c[i] = __float2int_rn(__fmul_rn(__fsub_rn(x[i], zf), inv_s));
+      c[i] = max(0, min(L, c[i]));
+    }
+    if (active) {
+      if constexpr (F == INT4A) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w |= static_cast<uint32_t>(c[i]) << (4 * i);
+        *reinterpret_cast<uint32_t*>(cache + row * (D / 2) + sub * 4) = w;
+      } else {
+        uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          w0 |= static_cast<uint32_t>(c[i]) << (8 * i);
+          w1 |= static_cast<uint32_t>(c[i + 4]) << (8 * i);
+        }
+        *reinterpret_cast<uint2*>(cache + row * D + sub * 8) = make_uint2(w0, w1);
+      }
+      if (sub == 0) {
+        constexpr int NF = KVARN ? 3 : 2;
+        __half* m = meta + ((static_cast<size_t>(blk) * Hkv + h) * NF) * bs + off;
+        m[0] = s16;
+        m[bs] = z16;
+        if constexpr (KVARN) m[2 * bs] = sig16;
+      }
+    }
+  }
+}
+
+template <int D, int KF, int VF, bool KVARN>
+__global__ void __launch_bounds__(kWriteWarps * 32)
+    write_cache_kernel(WriteArgs a) {
+  constexpr int LPR = RowGeom<D>::LPR;
+  constexpr int RPI = RowGeom<D>::RPI;
+  constexpr int U = 4;  // row groups loaded before any is processed
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kWriteWarps + (threadIdx.x >> 5);
+  if (t >= a.num_tokens) return;
+  const int64_t slot = a.slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= static_cast<int64_t>(a.num_blocks) * a.block_size) {
+    if (lane == 0) raise_error(1u);  // KVQ_DEVERR_SLOT_RANGE
+    return;
+  }
+  const int64_t blk = slot / a.block_size;
+  const int off = static_cast<int>(slot % a.block_size);
+  const int sub = lane % LPR, grp = lane / LPR;
+  const int Hkv = a.num_kv_heads;
+
+  uint32_t sign_bits = 0;
+  if constexpr (KVARN) {
+    if (a.signs != nullptr) {
+      const uint2 s = *reinterpret_cast<const uint2*>(a.signs + sub * 8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t byte = ((i < 4 ? s.x : s.y) >> (8 * (i & 3))) & 0xFFu;
+        sign_bits |= (byte & 0x80u) ? (1u << i) : 0u;
+      }
+    }
+  }
+
+  const uint16_t* krow = a.key + t * a.key_stride;
+  const uint16_t* vrow = a.value + t * a.value_stride;
+  const size_t row0 = (static_cast<size_t>(blk) * a.block_size + off) * Hkv;
+
+  for (int h0 = 0; h0 < Hkv; h0 += RPI * U) {
+    uint4 rk[U], rv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int h = h0 + u * RPI + grp;
+      rk[u] = h < Hkv ? ldg_stream16(krow + h * D + sub * 8) : make_uint4(0, 0, 0, 0);
+      rv[u] = h < Hkv ? ldg_stream16(vrow + h * D + sub * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int hb = h0 + u * RPI;
+      if (hb >= Hkv) break;
+      const int h = hb + grp;
+      const bool act = h < Hkv;
+      float x[8];
+      unpack8(rk[u], x);
+      quantize_store<D, KF, KVARN>(x, act, h, sub, row0 + h, a.k_cache, a.k_meta, a.k_inv, blk,
+                                   off, Hkv, a.block_size, sign_bits, a.cR);
+      unpack8(rv[u], x);
+      quantize_store<D, VF, KVARN>(x, act, h, sub, row0 + h, a.v_cache, a.v_meta, a.v_inv, blk,
+                                   off, Hkv, a.block_size, sign_bits, a.cR);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// per-tensor absmax calibration
+// ---------------------------------------------------------------------------
+__global__ void absmax_kernel(const uint16_t* __restrict__ x, int64_t n, unsigned* out) {
+  float m = 0.0f;
+  const int64_t nvec = n / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+       i += stride) {
+    const uint4 r = ldg_stream16(x + i * 8);
+    float v[8];
+    unpack8(r, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
+  }
+  for (int64_t i = nvec * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride)
+    m = fmaxf(m, fabsf(__uint_as_float(static_cast<uint32_t>(x[i]) << 16)));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(m));  // m >= 0: uint order
+}
+
+__global__ void scale_from_absmax_kernel(float* scale, float qmax) {
+  const float amax = __uint_as_float(*reinterpret_cast<unsigned*>(scale));
+  *scale = amax == 0.0f ? 1.0f : __fdiv_rn(amax, qmax);
+}
+
+template <int D, int KF, int VF, bool KVARN>
+cudaError_t launch_write_t(const WriteArgs& a, cudaStream_t st) {
+  const int64_t blocks = (a.num_tokens + kWriteWarps - 1) / kWriteWarps;
+  write_cache_kernel<D, KF, VF, KVARN><<<static_cast<unsigned>(blocks), kWriteWarps * 32, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch_write_d(const WriteArgs& a, int kf, int vf, bool kvarn, cudaStream_t st) {
+#define KVQ_W(KF_, VF_, KV_) \
+  if (kf == KF_ && vf == VF_ && kvarn == KV_) return launch_write_t<D, KF_, VF_, KV_>(a, st);
+  KVQ_W(INT8, INT8, false)
+  KVQ_W(INT8, E4M3, false)
+  KVQ_W(INT8, E5M2, false)
+  KVQ_W(E4M3, INT8, false)
+  KVQ_W(E4M3, E4M3, false)
+  KVQ_W(E4M3, E5M2, false)
+  KVQ_W(E5M2, INT8, false)
+  KVQ_W(E5M2, E4M3, false)
+  KVQ_W(E5M2, E5M2, false)
+  KVQ_W(INT4A, INT4A, false)
+  KVQ_W(INT4A, UINT8A, false)
+  KVQ_W(UINT8A, INT4A, false)
+  KVQ_W(UINT8A, UINT8A, false)
+  KVQ_W(INT4A, INT4A, true)
+  KVQ_W(INT4A, UINT8A, true)
+  KVQ_W(UINT8A, INT4A, true)
+  KVQ_W(UINT8A, UINT8A, true)
+#undef KVQ_W
+  return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+bool write_supported(int kf, int vf, bool kvarn) {
+  const bool sym_k = !is_asym(kf), sym_v = !is_asym(vf);
+  if (kvarn) return !sym_k && !sym_v;
+  return sym_k == sym_v;
+}
+
+cudaError_t launch_write(const WriteArgs& a, int head_dim, int kf, int vf, bool kvarn,
+                         cudaStream_t st) {
+  if (head_dim == 64) return dispatch_write_d<64>(a, kf, vf, kvarn, st);
+  if (head_dim == 128) return dispatch_write_d<128>(a, kf, vf, kvarn, st);
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_calibrate(const uint16_t* x, int64_t n, float qmax, float* scale,
+                             cudaStream_t st, int num_sms) {
+  cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  if (n > 0) {
+    const int64_t want = (n / 8 + 255) / 256;
+    const int blocks = static_cast<int>(want < 4LL * num_sms ? (want > 0 ? want : 1) : 4LL * num_sms);
+    absmax_kernel<<<blocks, 256, 0, st>>>(x, n, reinterpret_cast<unsigned*>(scale));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  scale_from_absmax_kernel<<<1, 1, 0, st>>>(scale, qmax);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -124,7 +124,7 @@ def _with_outliers(rng, x, channels_per_head, factor):
 
 
 def _per_token_magnitude(rng, x, sigma):
-    """Scale every (token, head) row by exp(N(0, sigma)) so row variances differ."""
+    """Scale every (token, head) row by exp(N(0, sigma)) so row norms differ."""
     t, hkv, _ = x.shape
     m = np.exp(rng.normal(0.0, sigma, size=(t, hkv, 1))).astype(np.float32)
     return x * m
@@ -150,6 +150,8 @@ def make_workload(
     spare_blocks: int = 4,
     context_lens: Optional[np.ndarray] = None,
 ) -> Workload:
+    # two independent streams: the paged layout (lengths, block permutation) and
+    # the tensor data, so that changing the block size keeps the same K/V/q
     rng = np.random.Generator(np.random.PCG64(seed))
     if context_lens is None:
         context_lens = rng.integers(ctx_lo, ctx_hi + 1, size=num_seqs).astype(np.int32)
@@ -158,13 +160,13 @@ def make_workload(
     table, nb = _paged_layout(rng, context_lens, block_size, spare_blocks)
     slots = slots_for_context(context_lens, table, block_size)
     t = int(slots.shape[0])
+    rng = np.random.Generator(np.random.PCG64([seed, 1]))
     key = _normal(rng, (t, num_kv_heads, head_dim))
     if k_outliers[0]:
         key = _with_outliers(rng, key, k_outliers[0], k_outliers[1])
     value = _normal(rng, (t, num_kv_heads, head_dim))
-    if token_magnitude_sigma:
+    if token_magnitude_sigma:  # keys only: values keep unit scale
         key = _per_token_magnitude(rng, key, token_magnitude_sigma)
-        value = _per_token_magnitude(rng, value, token_magnitude_sigma)
     query = _normal(rng, (num_seqs, num_q_heads, head_dim))
     signs = None
     if kvarn:

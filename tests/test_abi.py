@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_paged_kv_kvq_gb300 import build, kvq
+    build.build()
+    return kvq.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("kvq_write_cache", "kvq_paged_decode", "kvq_hadamard"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_entry_point(lib):
+    from quantized_paged_kv_kvq_gb300 import kvq
+    assert set(declared_functions()) == set(kvq.SIGNATURES)
+
+
+def test_status_strings(lib):
+    from quantized_paged_kv_kvq_gb300 import kvq
+    for code, name in kvq.STATUS.items():
+        assert lib.kvq_status_string(code).decode() == name
+    assert lib.kvq_version().decode().startswith("kvq")
+
+
+def _desc(**kw):
+    from quantized_paged_kv_kvq_gb300 import kvq
+    base = dict(k_fmt=1, v_fmt=1, num_kv_heads=8, head_dim=128, block_size=16, num_blocks=10,
+                flags=0, k_scale=0.1, v_scale=0.1, k_meta=None, v_meta=None, signs=None)
+    base.update(kw)
+    return kvq._CacheDesc(**base)
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _write(lib, desc, **kw):
+    a = dict(k=FAKE, v=FAKE, key=FAKE, value=FAKE, ks=1024, vs=1024, slots=FAKE, n=4)
+    a.update(kw)
+    return lib.kvq_write_cache(ctypes.byref(desc) if desc is not None else None, a["k"], a["v"],
+                               a["key"], a["value"], a["ks"], a["vs"], a["slots"], a["n"], None)
+
+
+def test_write_validation(lib):
+    ok_desc = _desc()
+    assert _write(lib, None) == 1
+    assert _write(lib, _desc(head_dim=96)) == 2
+    assert _write(lib, _desc(block_size=8)) == 2
+    assert _write(lib, _desc(k_fmt=9)) == 1
+    assert _write(lib, _desc(k_scale=0.0)) == 1
+    assert _write(lib, _desc(k_scale=float("nan"))) == 1
+    assert _write(lib, _desc(k_fmt=4, v_fmt=4)) == 1  # asymmetric needs meta
+    assert _write(lib, _desc(k_fmt=4, v_fmt=1, k_meta=FAKE)) == 2  # mixed families
+    assert _write(lib, _desc(flags=1)) == 2  # rotation needs asymmetric formats
+    assert _write(lib, _desc(flags=4)) == 1
+    assert _write(lib, ok_desc, k=None) == 1
+    assert _write(lib, ok_desc, key=FAKE + 2) == 1  # misaligned
+    assert _write(lib, ok_desc, ks=100) == 1  # stride shorter than a token
+    assert _write(lib, ok_desc, ks=1028) == 1  # stride not a multiple of 8
+    assert _write(lib, ok_desc, n=-1) == 1
+    assert _write(lib, ok_desc, n=0, k=None) == 0  # empty write is a no-op
+
+
+def _decode(lib, desc, **kw):
+    a = dict(k=FAKE, v=FAKE, out=FAKE, q=FAKE, s=4, hq=32, bt=FAKE, mb=64, cl=FAKE, mc=1024,
+             sm=0.088, p=256, ws=None, wsb=0)
+    a.update(kw)
+    return lib.kvq_paged_decode_ex(ctypes.byref(desc), a["k"], a["v"], a["out"], a["q"], a["s"],
+                                   a["hq"], a["bt"], a["mb"], a["cl"], a["mc"], a["sm"], a["p"],
+                                   a["ws"], a["wsb"], None)
+
+
+def test_decode_validation(lib):
+    d = _desc()
+    assert _decode(lib, d, hq=30) == 1  # not a multiple of the kv heads
+    assert _decode(lib, d, hq=8 * 16) == 2  # GQA ratio above 8
+    assert _decode(lib, d, p=100) == 1  # partition not a multiple of 64
+    assert _decode(lib, d, mb=10) == 1  # block table shorter than max context
+    assert _decode(lib, d, q=None) == 1
+    assert _decode(lib, d, sm=float("inf")) == 1
+    assert _decode(lib, d) == 3  # needs a workspace (4 partitions)
+    assert _decode(lib, d, ws=FAKE, wsb=10) == 3
+    n = ctypes.c_size_t(0)
+    assert lib.kvq_decode_workspace_size_ex(ctypes.byref(d), 4, 32, 1024, 256,
+                                            ctypes.byref(n)) == 0
+    assert n.value == 4 * 32 * 4 * (128 + 2) * 4
+    assert lib.kvq_decode_workspace_size_ex(ctypes.byref(d), 4, 32, 200, 256,
+                                            ctypes.byref(n)) == 0
+    assert n.value == 0  # one partition: no workspace
+    assert _decode(lib, d, s=0) == 0
+
+
+def test_hadamard_and_calibrate_validation(lib):
+    assert lib.kvq_hadamard(FAKE, 2, 10, 128, None, 0, None) == 1
+    assert lib.kvq_hadamard(FAKE, 0, 10, 96, None, 0, None) == 2
+    assert lib.kvq_hadamard(FAKE + 4, 0, 10, 128, None, 0, None) == 1
+    assert lib.kvq_hadamard(None, 0, 0, 128, None, 0, None) == 0
+    assert lib.kvq_calibrate_scale(FAKE, 10, 0.0, FAKE, None) == 1
+    assert lib.kvq_calibrate_scale(FAKE, -1, 127.0, FAKE, None) == 1

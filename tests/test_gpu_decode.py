@@ -1,0 +1,134 @@
+"""Paged-decode parity on the GPU against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from quantized_paged_kv_kvq_gb300 import kvq
+from quantized_paged_kv_kvq_gb300 import workloads as W
+
+from kvq_testing import GpuRun, OracleRun, assert_attention_close, out_numpy
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny_int8": dict(),
+    "llama8b_int8": dict(num_seqs=6, ctx_lo=1, ctx_hi=700),
+    "llama8b_e4m3k_int8v": dict(num_seqs=6, ctx_lo=1, ctx_hi=700),
+    "llama8b_e5m2": dict(num_seqs=6, ctx_lo=1, ctx_hi=700),
+    "llama70b_int4": dict(num_seqs=4, ctx_lo=1, ctx_hi=900),
+    "kvarn_131k": dict(num_seqs=3, ctx_lo=1, ctx_hi=900),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_decode_matches_oracle(name):
+    wl = W.workload(name, **SMALL[name])
+    g = GpuRun(wl)
+    g.write()
+    got = out_numpy(g.decode())
+    ref = OracleRun(wl).decode()
+    assert_attention_close(got, ref, name)
+    assert kvq.kvq_get_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["llama8b_int8", "llama70b_int4", "kvarn_131k",
+                                  "llama8b_e4m3k_int8v"])
+@pytest.mark.parametrize("partition", [64, 256, 2048, 0])
+def test_partition_size_invariance(name, partition):
+    """Split-K partitions of 64..2048 tokens (and the automatic choice) agree
+    with the oracle; sequences span several tiles, blocks and partitions."""
+    wl = W.workload(name, **dict(SMALL[name], ctx_lo=200, ctx_hi=2500))
+    g = GpuRun(wl)
+    g.write()
+    got = out_numpy(g.decode(partition_tokens=partition))
+    ref = OracleRun(wl).decode()
+    assert_attention_close(got, ref, f"{name} P={partition}")
+
+
+@pytest.mark.parametrize("name", ["llama8b_int8", "llama70b_int4", "kvarn_131k", "tiny_int8",
+                                  "llama8b_e5m2"])
+def test_context_length_edge_cases(name):
+    bs = W.WORKLOADS[name]["block_size"]
+    lens = np.array([0, 1, bs - 1, bs, bs + 1, 15, 16, 17, 63, 64, 65, 0, 2 * bs + 3], np.int32)
+    wl = W.workload(name, num_seqs=len(lens), context_lens=lens)
+    g = GpuRun(wl)
+    g.write()
+    ref = OracleRun(wl).decode()
+    for partition in (0, 64):
+        got = out_numpy(g.decode(partition_tokens=partition))
+        assert_attention_close(got, ref, f"{name} P={partition}")
+        assert np.all(got[lens == 0] == 0)
+
+
+def test_block_permutation_gives_identical_output():
+    wl = W.workload("llama8b_int8", num_seqs=4, ctx_lo=100, ctx_hi=600)
+    g = GpuRun(wl)
+    g.write()
+    out1 = g.decode(partition_tokens=256).clone()
+    perm = torch.from_numpy(np.random.default_rng(2).permutation(wl.num_blocks)).cuda()
+    kc2 = torch.empty_like(g.cache.k_cache)
+    vc2 = torch.empty_like(g.cache.v_cache)
+    kc2[perm] = g.cache.k_cache
+    vc2[perm] = g.cache.v_cache
+    g.cache.k_cache, g.cache.v_cache = kc2, vc2
+    bt = g.block_table.long()
+    g.block_table = torch.where(bt >= 0, perm[bt.clamp(min=0)], bt).int().contiguous()
+    out2 = g.decode(partition_tokens=256)
+    assert torch.equal(out1, out2)
+
+
+def test_block_size_16_and_32_agree():
+    lens = np.array([33, 100, 257, 5], np.int32)
+    outs = []
+    for bs in (16, 32):
+        wl = W.workload("llama8b_int8", num_seqs=4, context_lens=lens, block_size=bs)
+        g = GpuRun(wl)
+        g.write()
+        outs.append(out_numpy(g.decode()))
+        assert_attention_close(outs[-1], OracleRun(wl).decode(), f"bs={bs}")
+    assert_attention_close(outs[0], outs[1], "bs16 vs bs32")
+
+
+def test_bad_block_id_is_flagged_not_faulted():
+    wl = W.workload("tiny_int8")
+    g = GpuRun(wl)
+    g.write()
+    bt = g.block_table.clone()
+    bt[0, 0] = wl.num_blocks + 100  # outside the cache
+    g.block_table = bt
+    g.decode()
+    assert kvq.kvq_get_device_error() & kvq.DEVERR_BLOCK_RANGE
+    assert kvq.kvq_get_device_error() == 0
+
+
+def test_decode_is_deterministic():
+    wl = W.workload("llama70b_int4", num_seqs=3, ctx_lo=500, ctx_hi=1500)
+    g = GpuRun(wl)
+    g.write()
+    a = g.decode().clone()
+    b = g.decode()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["llama8b_int8", "llama8b_e4m3k_int8v", "llama8b_e5m2",
+                                  "llama70b_int4", "kvarn_131k"])
+def test_decode_full_size_sampled(name):
+    """The full-size workload, written and decoded in the launch configuration
+    the benchmark times; a sample of (sequence, kv-head) pairs is computed by
+    the oracle from its own cache of those sequences."""
+    wl = W.workload(name)
+    g = GpuRun(wl)
+    g.write()
+    got = out_numpy(g.decode())
+    rng = np.random.default_rng(7)
+    seqs = sorted(rng.choice(wl.num_seqs, size=min(2, wl.num_seqs), replace=False).tolist())
+    heads = sorted(rng.choice(wl.num_kv_heads, size=2, replace=False).tolist())
+    pairs = [(s, h) for s in seqs for h in heads]
+    ref = OracleRun(wl, seqs=seqs).decode(pairs=pairs)
+    gq = wl.gqa
+    rows = [(s, h * gq + j) for s, h in pairs for j in range(gq)]
+    sel_got = np.stack([got[s, q] for s, q in rows])
+    sel_ref = np.stack([ref[s, q] for s, q in rows])
+    assert_attention_close(sel_got, sel_ref, name)
+    assert np.all(np.isfinite(got))
+    assert kvq.kvq_get_device_error() == 0

@@ -80,7 +80,9 @@ def test_written_rows_dequantize_close_to_inputs():
                                    wl.kvarn, wl.signs, wl.head_dim)
             ref = wl.key[start:start + ctx, 0].astype(np.float64)
             rel = np.linalg.norm(k - ref) / max(np.linalg.norm(ref), 1e-30)
-            assert rel < (0.3 if wl.k_fmt == "int4_asym" else 0.07), (name, rel)
+            # int4 with outlier channels is coarse; e5m2 keeps 2 mantissa bits
+            bound = {"int4_asym": 0.3, "fp8_e5m2": 0.1}.get(wl.k_fmt, 0.07)
+            assert rel < bound, (name, rel)
 
 
 def test_unwritten_slots_keep_poison():
