@@ -204,6 +204,43 @@ kvq_status kvq_paged_decode_combine(const kvq_cache_desc* cache, const void* k_c
                                     size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * kvq_paged_decode_static -- kvq_paged_decode_ex for callers that cannot
+ * allocate device memory.  None of the source pages has a counterpart of
+ * this entry point: it exists for integration, not for the method.
+ *
+ * Who needs it: code that must not call cudaMalloc (or any allocator) once it
+ * is running -- a plugin inside a host application or framework that owns
+ * every byte of device memory through its own pool, or a latency-bound
+ * serving loop where an allocation could block on the device or fail late.
+ * Such a caller still owns the cache, query and output buffers, but has no way
+ * to obtain the split-K workspace.
+ *
+ * Instead of a workspace, the call uses a scratch array of
+ * kvq_paged_decode_static_capacity() bytes (16 MiB) compiled into the library:
+ * every GPU that loads the library holds that memory until the process exits.
+ * Sizes whose workspace (kvq_decode_workspace_size_ex) exceeds it return
+ * KVQ_ERR_WORKSPACE before anything is launched.  The call allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * The first call on a device looks up the scratch's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array, and it keeps whatever the last
+ * call left: nothing in it needs to start at zero (every value the combine
+ * reads is written earlier in the same call), but two calls whose kernels
+ * overlap on the GPU (different streams, or several host threads) race on it
+ * and corrupt each other's results -- serialize them.
+ * Arguments and results are those of kvq_paged_decode_ex.
+ */
+kvq_status kvq_paged_decode_static(const kvq_cache_desc* cache, const void* k_cache,
+                                   const void* v_cache, void* out, const void* query,
+                                   int32_t num_seqs, int32_t num_q_heads,
+                                   const int32_t* block_table, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int32_t max_context_len,
+                                   float sm_scale, int32_t partition_tokens, kvq_stream_t stream);
+/* Bytes of the scratch array kvq_paged_decode_static uses. */
+size_t kvq_paged_decode_static_capacity(void);
+
+/*
  * kvq_hadamard -- in-place orthonormal Walsh-Hadamard rotation of `rows`
  * rows of `head_dim` elements (KVarN article, 'Contexte Technique').
  *   forward (inverse = 0): x <- cR * H (d . x)

@@ -59,6 +59,9 @@ SIGNATURES = {
                                            _F32, _I32, _P, _SZ, _P]),
     "kvq_paged_decode_combine": (_I32, [_DESC, _P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _I32,
                                         _F32, _I32, _P, _SZ, _P]),
+    "kvq_paged_decode_static": (_I32, [_DESC, _P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _I32,
+                                       _F32, _I32, _P]),
+    "kvq_paged_decode_static_capacity": (_SZ, []),
     "kvq_hadamard": (_I32, [_P, _I32, _I64, _I32, _P, _I32, _P]),
     "kvq_calibrate_scale": (_I32, [_P, _I64, _F32, _P, _P]),
     "kvq_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -237,6 +240,32 @@ def kvq_paged_decode_combine(cache, query, out, block_table, context_lens, max_c
     return _decode_call("kvq_paged_decode_combine", cache, query, out, block_table,
                         context_lens, max_context_len, sm_scale, workspace, partition_tokens,
                         stream)
+
+
+def kvq_paged_decode_static(cache: KVCache, query: torch.Tensor, out: torch.Tensor,
+                            block_table: torch.Tensor, context_lens: torch.Tensor,
+                            max_context_len: int, sm_scale: float, partition_tokens: int = 0,
+                            stream=None) -> torch.Tensor:
+    """kvq_paged_decode for callers that cannot allocate: the split-K scratch is
+    the library's own fixed array (kvq_paged_decode_static_capacity() bytes)
+    instead of a workspace tensor.  Calls that overlap on the GPU race on it."""
+    lib = load_library()
+    assert query.dtype == torch.bfloat16 and out.dtype == torch.bfloat16
+    assert query.is_contiguous() and out.is_contiguous()
+    assert block_table.dtype == torch.int32 and context_lens.dtype == torch.int32
+    assert block_table.is_contiguous()
+    s, hq, _ = query.shape
+    d = cache.desc()
+    st = lib.kvq_paged_decode_static(ctypes.byref(d), _ptr(cache.k_cache), _ptr(cache.v_cache),
+                                     _ptr(out), _ptr(query), s, hq, _ptr(block_table),
+                                     block_table.shape[1], _ptr(context_lens), max_context_len,
+                                     float(sm_scale), partition_tokens, _stream(stream))
+    _check(st, "kvq_paged_decode_static")
+    return out
+
+
+def kvq_paged_decode_static_capacity() -> int:
+    return int(load_library().kvq_paged_decode_static_capacity())
 
 
 def kvq_hadamard(x: torch.Tensor, signs: Optional[torch.Tensor] = None, inverse: bool = False,
