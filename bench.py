@@ -4,8 +4,10 @@
 One step = the whole path on one batch of synthetic input: quantize-and-
 scatter every context token into the paged cache (kvq_write_cache), then
 single-token paged decode over it (kvq_paged_decode, its partition and
-combine launches timed separately).  Inputs are resident in HBM before the
-timed region; L2 is flushed (a 2x-L2 memset) before every timed kernel group,
+one launch; the last CTA of each (sequence, kv-head) merges the
+split-K partitions).  Inputs are resident in HBM before the
+timed region; L2 is flushed (a 2x-L2 memset, then a 2x-L2 read) before every
+timed kernel group,
 outside the CUDA-event pairs.  One JSON line on stdout (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
@@ -356,24 +358,29 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
     ws_bytes = kvq.kvq_decode_workspace_size(cache, wl.num_seqs, wl.num_q_heads,
                                              wl.max_context_len, P)
     ws = torch.empty(max(ws_bytes, 16) // 4 + 4, dtype=torch.float32, device=dev)
-    multi = ws_bytes > 0
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    # L2 flush: write one buffer of 2x L2, then read another of 2x L2, so the
+    # timed kernels start with an L2 that holds none of their data and no dirty
+    # lines (whose write-back would otherwise land inside the next timed kernel)
+    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        flush_r.sum()
     dargs = (cache, query, out, block_table, ctx_lens, wl.max_context_len, sm_scale, ws, P)
 
     def step(ev):
-        flush.zero_()
+        flush_l2()
         ev[0].record()
         kvq.kvq_write_cache(cache, key, value, slots)
         ev[1].record()
-        flush.zero_()
+        flush_l2()
         ev[2].record()
-        kvq.kvq_paged_decode_partitions(*dargs)
+        kvq.kvq_paged_decode(*dargs)
         ev[3].record()
-        kvq.kvq_paged_decode_combine(*dargs)
-        ev[4].record()
 
-    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for _ in range(args.warmup):
         step(mk())
     torch.cuda.synchronize()
@@ -395,18 +402,16 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
     wall = time.perf_counter() - w0
     clocks = sampler.stop()
     t_write = sum(e[0].elapsed_time(e[1]) for e in events) / 1e3
-    t_part = sum(e[2].elapsed_time(e[3]) for e in events) / 1e3
-    t_comb = sum(e[3].elapsed_time(e[4]) for e in events) / 1e3
-    t_dec = t_part + t_comb
-    times = torch.tensor([t_write, t_dec, t_part, wall], dtype=torch.float64, device=dev)
+    t_dec = sum(e[2].elapsed_time(e[3]) for e in events) / 1e3
+    times = torch.tensor([t_write, t_dec, wall], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_write, t_dec, t_part, wall = times.tolist()
+    t_write, t_dec, wall = times.tolist()
     dbytes, wbytes = decode_bytes(wl), write_bytes(wl)
     K = args.steps
     gbs = aggregate([t_dec], [world * dbytes * K]) / 1e9
     hbm, peak_src = measured_peaks()
-    achieved = dbytes / (t_part / K) / 1e9
+    achieved = dbytes / (t_dec / K) / 1e9
 
     # end to end through the public API: pinned host inputs in, result out
     e2e = None
@@ -449,7 +454,7 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
         return
     cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_subprocess(
         args.workload, args.cpu_seconds)
-    launches = K * (2 + (1 if multi else 0))
+    launches = 2 * K  # one write and one decode launch per step
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": 1e3 * (t_write + t_dec) / K,
@@ -460,10 +465,10 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
                    "head_dim": wl.head_dim, "block_size": wl.block_size,
                    "k_fmt": wl.k_fmt, "v_fmt": wl.v_fmt, "kvarn": wl.kvarn,
                    "context_tokens": int(wl.context_lens.sum()),
-                   "partition_tokens": P or "auto", "l2": "flushed (2xL2 memset) before "
-                   "the write and before the decode, outside the timed events"},
+                   "partition_tokens": P or "auto", "l2": "flushed before the write and before the decode (2xL2 memset, "
+                   "then a 2xL2 read), outside the timed events"},
         "decode_tok_s": world * wl.num_seqs * K / t_dec,
-        "decode_us": 1e6 * t_dec / K, "decode_partition_us": 1e6 * t_part / K,
+        "decode_us": 1e6 * t_dec / K, "decode_partitions": ws_bytes > 0,
         "cache_write_tok_s": world * wl.num_tokens * K / t_write,
         "cache_write_gbs": world * wbytes * K / t_write / 1e9,
         "cache_write_us": 1e6 * t_write / K,

@@ -150,7 +150,11 @@ kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_se
  *   context_len 0 gives out = 0.
  * sm_scale: logits are sm_scale * <q, k>.
  * workspace: device memory of >= kvq_decode_workspace_size(...) bytes
- *   (may be NULL when that size is 0), 16-byte aligned, contents ignored.
+ *   (may be NULL when that size is 0), 16-byte aligned; its contents on entry
+ *   do not matter (completion counters inside it carry a per-call tag).  Two
+ *   calls that overlap on the GPU must not share a workspace.
+ * One kernel launch: CTAs of (kv-head, sequence, context partition); the last
+ *   CTA to finish a (sequence, kv-head) merges its partitions (log-sum-exp).
  * out[s, h] = sum_t softmax_t(sm_scale <q, k_t>) v_t over the dequantized
  *   cache, computed with fp32 softmax and fp32 accumulation (keys and values
  *   enter the tensor cores as exact fp16 code values; the query is rounded to
@@ -165,8 +169,9 @@ kvq_status kvq_paged_decode(const kvq_cache_desc* cache, const void* k_cache,
 
 /*
  * kvq_paged_decode_ex -- kvq_paged_decode with an explicit context
- * partition size (tokens per split-K partition, a multiple of 64; 0 = the
- * automatic choice).  The workspace must hold
+ * partition size (tokens per split-K partition, a multiple of 64, at most
+ * 8192; 0 = the automatic choice); sizes that need more than 512 partitions
+ * per sequence return KVQ_ERR_UNSUPPORTED.  The workspace must hold
  * kvq_decode_workspace_size_ex(...) bytes for the same partition size.
  */
 kvq_status kvq_decode_workspace_size_ex(const kvq_cache_desc* cache, int32_t num_seqs,
@@ -179,29 +184,6 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
                                const int32_t* context_lens, int32_t max_context_len,
                                float sm_scale, int32_t partition_tokens, void* workspace,
                                size_t workspace_bytes, kvq_stream_t stream);
-
-/*
- * The two launches of kvq_paged_decode_ex, callable separately with the same
- * arguments (e.g. to time them, or to run the combine later on the stream):
- * kvq_paged_decode_partitions runs the per-partition attention (and, when one
- * partition covers every sequence, writes `out` itself); kvq_paged_decode_combine
- * merges the partitions into `out` (a no-op with one partition).  Calling
- * partitions then combine on one stream equals one kvq_paged_decode_ex call.
- */
-kvq_status kvq_paged_decode_partitions(const kvq_cache_desc* cache, const void* k_cache,
-                                       const void* v_cache, void* out, const void* query,
-                                       int32_t num_seqs, int32_t num_q_heads,
-                                       const int32_t* block_table, int32_t max_blocks_per_seq,
-                                       const int32_t* context_lens, int32_t max_context_len,
-                                       float sm_scale, int32_t partition_tokens, void* workspace,
-                                       size_t workspace_bytes, kvq_stream_t stream);
-kvq_status kvq_paged_decode_combine(const kvq_cache_desc* cache, const void* k_cache,
-                                    const void* v_cache, void* out, const void* query,
-                                    int32_t num_seqs, int32_t num_q_heads,
-                                    const int32_t* block_table, int32_t max_blocks_per_seq,
-                                    const int32_t* context_lens, int32_t max_context_len,
-                                    float sm_scale, int32_t partition_tokens, void* workspace,
-                                    size_t workspace_bytes, kvq_stream_t stream);
 
 /*
  * kvq_paged_decode_static -- kvq_paged_decode_ex for callers that cannot
@@ -268,6 +250,7 @@ kvq_status kvq_calibrate_scale(const void* x, int64_t n, float qmax, float* scal
 #define KVQ_DEVERR_SLOT_RANGE 1u  /* a slot id past num_blocks*block_size */
 #define KVQ_DEVERR_BLOCK_RANGE 2u /* a block-table entry outside [0, num_blocks) */
 #define KVQ_DEVERR_CONTEXT_RANGE 4u /* a context length outside [0, max_context_len] */
+#define KVQ_DEVERR_COMBINE 8u       /* a partition-merge counter update gave up */
 
 /*
  * kvq_get_device_error -- synchronizes `stream`, then reads and clears the

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <chrono>
 
 #include "../../include/kvq.h"
 #include "kvq_device.cuh"
@@ -75,16 +76,32 @@ int auto_partition(int num_seqs, int hkv, int max_ctx, int sms) {
   p = ((p + 63) / 64) * 64;
   if (p < 256) p = 256;
   if (p > kMaxPartition) p = kMaxPartition;
+  const long long floor_np = ((max_ctx + kMaxPartitions - 1) / kMaxPartitions + 63) / 64 * 64;
+  if (p < floor_np) p = floor_np;  // at most kMaxPartitions partitions per sequence
   const long long whole = ((max_ctx + 63) / 64) * 64;
   if (p >= whole && whole <= kMaxPartition) p = whole;
   return static_cast<int>(p);
 }
 
-size_t workspace_bytes_for(int num_seqs, int hq, int d, int np) {
+// Workspace: partial accumulators [S, Hq, NP, D] f32, (max, sum) [S, Hq, NP, 2]
+// f32, then one 64-bit completion counter per (sequence, kv-head).
+size_t workspace_bytes_for(int num_seqs, int hq, int hkv, int d, int np) {
   if (np <= 1) return 0;
   const size_t rows = static_cast<size_t>(num_seqs) * hq * np;
-  const size_t acc = rows * d * sizeof(float);
-  return acc + rows * 2 * sizeof(float);
+  return rows * (d + 2) * sizeof(float) + static_cast<size_t>(num_seqs) * hkv * 8;
+}
+
+// 48-bit tag, different for every decode call of the process, so that the
+// completion counters never need clearing between calls.
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> counter{0};
+  static const unsigned long long base = [] {
+    unsigned long long x = static_cast<unsigned long long>(
+        std::chrono::steady_clock::now().time_since_epoch().count());
+    x ^= reinterpret_cast<uintptr_t>(&counter) * 0x9E3779B97F4A7C15ull;
+    return x;
+  }();
+  return (base + counter.fetch_add(1)) & 0xFFFFFFFFFFFFull;
 }
 
 kvq_status decode_shape(const kvq_cache_desc* c, int32_t num_seqs, int32_t num_q_heads,
@@ -103,7 +120,7 @@ kvq_status decode_shape(const kvq_cache_desc* c, int32_t num_seqs, int32_t num_q
     p = auto_partition(num_seqs, c->num_kv_heads, max_context_len, sms);
   }
   const int np = max_context_len > 0 ? ceil_div(max_context_len, p) : 1;
-  if (np > 65535 || num_seqs > 65535) return KVQ_ERR_UNSUPPORTED;
+  if (np > kMaxPartitions || num_seqs > 65535) return KVQ_ERR_UNSUPPORTED;
   *P = p;
   *NP = np;
   return KVQ_OK;
@@ -177,7 +194,7 @@ kvq_status kvq_decode_workspace_size_ex(const kvq_cache_desc* cache, int32_t num
   kvq_status st =
       decode_shape(cache, num_seqs, num_q_heads, max_context_len, partition_tokens, &P, &NP);
   if (st != KVQ_OK) return st;
-  *bytes = workspace_bytes_for(num_seqs, num_q_heads, cache->head_dim, NP);
+  *bytes = workspace_bytes_for(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, NP);
   return KVQ_OK;
 }
 
@@ -187,14 +204,12 @@ kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_se
   return kvq_decode_workspace_size_ex(cache, num_seqs, num_q_heads, max_context_len, 0, bytes);
 }
 
-namespace {
-
-kvq_status paged_decode_impl(const kvq_cache_desc* cache, const void* k_cache, const void* v_cache,
-                             void* out, const void* query, int32_t num_seqs, int32_t num_q_heads,
-                             const int32_t* block_table, int32_t max_blocks_per_seq,
-                             const int32_t* context_lens, int32_t max_context_len, float sm_scale,
-                             int32_t partition_tokens, void* workspace, size_t workspace_bytes,
-                             kvq_stream_t stream, int phase) {
+kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
+                               const void* v_cache, void* out, const void* query,
+                               int32_t num_seqs, int32_t num_q_heads, const int32_t* block_table,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t max_context_len, float sm_scale, int32_t partition_tokens,
+                               void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
   int P = 0, NP = 0;
   kvq_status st =
       decode_shape(cache, num_seqs, num_q_heads, max_context_len, partition_tokens, &P, &NP);
@@ -208,7 +223,8 @@ kvq_status paged_decode_impl(const kvq_cache_desc* cache, const void* k_cache, c
   if (max_blocks_per_seq < ceil_div(max_context_len, cache->block_size) || max_blocks_per_seq < 0)
     return KVQ_ERR_INVALID_ARGUMENT;
   if (!isfinite(sm_scale)) return KVQ_ERR_INVALID_ARGUMENT;
-  const size_t need = workspace_bytes_for(num_seqs, num_q_heads, cache->head_dim, NP);
+  const size_t need =
+      workspace_bytes_for(num_seqs, num_q_heads, cache->num_kv_heads, cache->head_dim, NP);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return KVQ_ERR_WORKSPACE;
   if (need > 0 && !aligned(workspace, 16)) return KVQ_ERR_INVALID_ARGUMENT;
   const bool kvarn = (cache->flags & KVQ_FLAG_VARNORM_ROTATE) != 0;
@@ -225,11 +241,14 @@ kvq_status paged_decode_impl(const kvq_cache_desc* cache, const void* k_cache, c
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * NP;
   a.ws_acc = need ? static_cast<float*>(workspace) : nullptr;
   a.ws_ml = need ? static_cast<float*>(workspace) + rows * cache->head_dim : nullptr;
+  a.counters = need ? reinterpret_cast<unsigned long long*>(a.ws_ml + rows * 2) : nullptr;
+  a.epoch = next_epoch();
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = cache->num_kv_heads;
   a.gqa = num_q_heads / cache->num_kv_heads;
   a.block_size = cache->block_size;
+  a.block_shift = cache->block_size == 16 ? 4 : 5;
   a.num_blocks = cache->num_blocks;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.max_context_len = max_context_len;
@@ -238,7 +257,6 @@ kvq_status paged_decode_impl(const kvq_cache_desc* cache, const void* k_cache, c
   a.qk_scale = sm_scale * kLog2e * (is_asym(cache->k_fmt) ? 1.0f : cache->k_scale);
   a.v_scale = is_asym(cache->v_fmt) ? 1.0f : cache->v_scale;
   a.cR = rotation_scale(cache->head_dim);
-  a.phase = phase;
   cudaError_t e;
   const int kf = cache->k_fmt, vf = cache->v_fmt;
   if (is_asym(kf)) {
@@ -250,43 +268,6 @@ kvq_status paged_decode_impl(const kvq_cache_desc* cache, const void* k_cache, c
   }
   if (e == cudaErrorNotSupported) return KVQ_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
-}
-
-}  // namespace
-
-kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
-                               const void* v_cache, void* out, const void* query,
-                               int32_t num_seqs, int32_t num_q_heads, const int32_t* block_table,
-                               int32_t max_blocks_per_seq, const int32_t* context_lens,
-                               int32_t max_context_len, float sm_scale, int32_t partition_tokens,
-                               void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
-  return paged_decode_impl(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
-                           max_blocks_per_seq, context_lens, max_context_len, sm_scale,
-                           partition_tokens, workspace, workspace_bytes, stream, 3);
-}
-
-kvq_status kvq_paged_decode_partitions(const kvq_cache_desc* cache, const void* k_cache,
-                                       const void* v_cache, void* out, const void* query,
-                                       int32_t num_seqs, int32_t num_q_heads,
-                                       const int32_t* block_table, int32_t max_blocks_per_seq,
-                                       const int32_t* context_lens, int32_t max_context_len,
-                                       float sm_scale, int32_t partition_tokens, void* workspace,
-                                       size_t workspace_bytes, kvq_stream_t stream) {
-  return paged_decode_impl(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
-                           max_blocks_per_seq, context_lens, max_context_len, sm_scale,
-                           partition_tokens, workspace, workspace_bytes, stream, 1);
-}
-
-kvq_status kvq_paged_decode_combine(const kvq_cache_desc* cache, const void* k_cache,
-                                    const void* v_cache, void* out, const void* query,
-                                    int32_t num_seqs, int32_t num_q_heads,
-                                    const int32_t* block_table, int32_t max_blocks_per_seq,
-                                    const int32_t* context_lens, int32_t max_context_len,
-                                    float sm_scale, int32_t partition_tokens, void* workspace,
-                                    size_t workspace_bytes, kvq_stream_t stream) {
-  return paged_decode_impl(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
-                           max_blocks_per_seq, context_lens, max_context_len, sm_scale,
-                           partition_tokens, workspace, workspace_bytes, stream, 2);
 }
 
 kvq_status kvq_paged_decode(const kvq_cache_desc* cache, const void* k_cache,

@@ -32,6 +32,7 @@
 namespace kvq {
 
 constexpr int kDecodeWarps = 4;
+constexpr int kDecodeMinBlocks = 4;  // resident CTAs per SM the register budget targets
 
 template <int D, int KF, int VF, bool KVARN>
 struct DecodeCfg {
@@ -52,13 +53,15 @@ struct DecodeCfg {
   static constexpr int V_BYTES = 4 * 32 * VPS;
   static constexpr int M_BYTES = (KMF + VMF) * 32;
   static constexpr int STAGE = K_BYTES + V_BYTES + M_BYTES;
-  static constexpr int STAGES = STAGE >= 4096 ? 4 : 6;
+  static constexpr int STAGES = STAGE >= 4096 ? 3 : STAGE >= 3072 ? 4 : STAGE >= 2048 ? 5 : 8;
   static constexpr int WARP_SMEM = STAGES * STAGE;
   static constexpr int RING = kDecodeWarps * WARP_SMEM;
-  static constexpr int COMBINE = kDecodeWarps * 8 * (D + 2) * 4 + 8 * D * 4;
+  static constexpr int COMBINE = kDecodeWarps * 8 * (D + 2) * 4 + 8 * D * 4;  // warps
+  static constexpr int MERGE = (8 * kMaxPartitions + 8 + 8 * D) * 4;        // partitions
   static constexpr int QAREA = 8 * D * 4;
-  static constexpr int MAIN = RING > COMBINE ? (RING > QAREA ? RING : QAREA)
-                                             : (COMBINE > QAREA ? COMBINE : QAREA);
+  static constexpr int max2(int x, int y) { return x > y ? x : y; }
+  // rings and the query rows live side by side; the combines reuse it all later
+  static constexpr int MAIN = max2(RING + QAREA, max2(COMBINE, MERGE));
   static constexpr int SMEM = MAIN + (kMaxPartition / 16) * 4;
   static_assert(KW * 4 == K_LANE && VW * 4 == VPS, "layout");
 };
@@ -175,7 +178,7 @@ __device__ __forceinline__ uint16_t f2bf(float x) {
 }
 
 template <int D, int KF, int VF, bool KVARN>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 3)
+__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeMinBlocks)
     decode_partition_kernel(const DecodeArgs a) {
   using C = DecodeCfg<D, KF, VF, KVARN>;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -188,26 +191,27 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
     if (threadIdx.x == 0 && h == 0 && p == 0) raise_error(4u);  // KVQ_DEVERR_CONTEXT_RANGE
     ctx = ctx < 0 ? 0 : a.max_context_len;
   }
-  const int t_begin = p * a.partition_tokens;
+  const int P = a.partition_tokens;
+  const int t_begin = p * P;
   const bool direct = a.num_partitions == 1;
   const size_t out_row0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G;
 
   if (t_begin >= ctx) {
-    if (direct && p == 0) {
+    if (p == 0) {  // empty context: the output is zero
       for (int i = threadIdx.x; i < G * D; i += blockDim.x) a.out[out_row0 * D + i] = 0;
     }
     return;
   }
-  const int len = min(ctx - t_begin, a.partition_tokens);
+  const int len = min(ctx - t_begin, P);
   const int ntiles = (len + 15) >> 4;
   const int Hkv = a.num_kv_heads;
+  const int bs_shift = a.block_shift, bs_mask = a.block_size - 1;
 
   // ---- block ids of this partition
   int* s_blk = reinterpret_cast<int*>(smem + C::MAIN);
   {
-    const int nblk = (len + a.block_size - 1) / a.block_size;
-    const int* bt = a.block_table + static_cast<size_t>(s) * a.max_blocks_per_seq +
-                    t_begin / a.block_size;
+    const int nblk = (len + bs_mask) >> bs_shift;
+    const int* bt = a.block_table + static_cast<size_t>(s) * a.max_blocks_per_seq + (t_begin >> bs_shift);
     for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
       int b = bt[i];
       if (b < 0 || b >= a.num_blocks) {
@@ -217,8 +221,56 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
       s_blk[i] = b;
     }
   }
+  __syncthreads();
+
+  // ---- per-warp pipeline over tiles warp, warp + W, ...; the first tiles are
+  // requested before the query is prepared so that the two overlap
+  uint8_t* ring = smem + warp * C::WARP_SMEM;
+  const uint32_t ring_s = smem_u32(ring);
+  const int my_tiles = ntiles > warp ? (ntiles - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
+  const uint32_t rowK = static_cast<uint32_t>(Hkv) * C::KB;  // bytes from one token row to the next
+  const uint32_t rowV = static_cast<uint32_t>(Hkv) * C::VB;
+  const uint32_t lane_k = 2 * g * rowK + h * C::KB + c * C::KPS;
+  const uint32_t lane_v = 4 * c * rowV + h * C::VB + g * C::VPS;
+
+  auto issue = [&](int it, int stage) {
+    const int tok0 = (warp + it * kDecodeWarps) * 16;
+    const int blk = s_blk[tok0 >> bs_shift];
+    const size_t trow = (static_cast<size_t>(blk) << bs_shift) + (tok0 & bs_mask);
+    const uint8_t* kb = a.k_cache + trow * rowK + lane_k;
+    const uint8_t* vb = a.v_cache + trow * rowV + lane_v;
+    const uint32_t st = ring_s + stage * C::STAGE;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+#pragma unroll
+      for (int pc = 0; pc < C::KP; ++pc)
+        cp_async<C::KPS>(st + ((r * C::KP + pc) * 32 + lane) * C::KPS, kb + r * rowK + pc * C::KSTRIDE_P);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      cp_async<C::VPS>(st + C::K_BYTES + (u * 32 + lane) * C::VPS, vb + u * rowV);
+    if constexpr (C::KMF + C::VMF > 0) {
+      if (lane < 2 * (C::KMF + C::VMF)) {
+        const int fidx = lane >> 1, half = lane & 1;
+        const bool isk = fidx < C::KMF;
+        const int f = isk ? fidx : fidx - C::KMF;
+        const int nf = isk ? C::KMF : C::VMF;
+        const __half* base = isk ? a.k_meta : a.v_meta;
+        const __half* src = base + ((static_cast<size_t>(blk) * Hkv + h) * nf + f) * a.block_size +
+                            (tok0 & bs_mask) + 8 * half;
+        cp_async<16>(st + C::K_BYTES + C::V_BYTES + fidx * 32 + half * 16, src);
+      }
+    }
+  };
+
+#pragma unroll
+  for (int i = 0; i < C::STAGES - 1; ++i) {
+    if (i < my_tiles) issue(i, i);
+    cp_async_commit();
+  }
+
   // ---- query rows (fp32) of the G heads, rotated for KVarN
-  float* sq = reinterpret_cast<float*>(smem);
+  float* sq = reinterpret_cast<float*>(smem + C::RING);
   for (int i = threadIdx.x; i < 8 * D; i += blockDim.x) {
     const int n = i / D;
     float v = 0.0f;
@@ -247,60 +299,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
   qs += __shfl_xor_sync(0xffffffffu, qs, 2);
   const float qsum0 = __shfl_sync(0xffffffffu, qs, (2 * c) * 4);
   const float qsum1 = __shfl_sync(0xffffffffu, qs, (2 * c + 1) * 4);
-  __syncthreads();  // query area is reused by the rings below
-
-  // ---- per-warp pipeline over tiles warp, warp + W, ...
-  uint8_t* ring = smem + warp * C::WARP_SMEM;
-  const uint32_t ring_s = smem_u32(ring);
-  const int my_tiles = ntiles > warp ? (ntiles - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
-
-  auto issue = [&](int it, int stage) {
-    const int tok0 = (warp + it * kDecodeWarps) * 16;
-    const int64_t blk = s_blk[tok0 / a.block_size];
-    const int off0 = tok0 % a.block_size;
-    const size_t row0 = (static_cast<size_t>(blk) * a.block_size + off0) * Hkv + h;
-    const uint32_t st = ring_s + stage * C::STAGE;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const uint8_t* src = a.k_cache + (row0 + static_cast<size_t>(2 * g + r) * Hkv) * C::KB + c * C::KPS;
-#pragma unroll
-      for (int pc = 0; pc < C::KP; ++pc)
-        cp_async<C::KPS>(st + ((r * C::KP + pc) * 32 + lane) * C::KPS, src + pc * C::KSTRIDE_P);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint8_t* src = a.v_cache + (row0 + static_cast<size_t>(4 * c + u) * Hkv) * C::VB + g * C::VPS;
-      cp_async<C::VPS>(st + C::K_BYTES + (u * 32 + lane) * C::VPS, src);
-    }
-    if constexpr (C::KMF + C::VMF > 0) {
-      if (lane < 2 * (C::KMF + C::VMF)) {
-        const int fidx = lane >> 1, half = lane & 1;
-        const bool isk = fidx < C::KMF;
-        const int f = isk ? fidx : fidx - C::KMF;
-        const int nf = isk ? C::KMF : C::VMF;
-        const __half* base = isk ? a.k_meta : a.v_meta;
-        const __half* src =
-            base + ((static_cast<size_t>(blk) * Hkv + h) * nf + f) * a.block_size + off0 + 8 * half;
-        cp_async<16>(st + C::K_BYTES + C::V_BYTES + fidx * 32 + half * 16, src);
-      }
-    }
-  };
-
-#pragma unroll
-  for (int i = 0; i < C::STAGES - 1; ++i) {
-    if (i < my_tiles) issue(i, i);
-    cp_async_commit();
-  }
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
   float O[C::DTILES][4];
 #pragma unroll
   for (int i = 0; i < C::DTILES; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
 
+  int stage = 0;
   for (int it = 0; it < my_tiles; ++it) {
     cp_async_wait<C::STAGES - 2>();
     __syncwarp();
-    const int stage = it % C::STAGES;
     const uint8_t* st = ring + stage * C::STAGE;
     const int valid = len - (warp + it * kDecodeWarps) * 16;
 
@@ -324,6 +332,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
         for (int k = 0; k < C::KW; ++k) kw[r][k] ^= 0x80808080u;
       }
     }
+
+    // ---- S^T = K q^T (two accumulators halve the dependent mma chain)
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < C::KSTEPS; ++j) {
+      uint32_t a0, a1, a2, a3;
+      k_frag<KF, C::KW>(kw, j, a0, a1, a2, a3);
+      if (j & 1) mma16816(sb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+      else mma16816(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+    }
+    float sacc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sacc[k] = sa[k] + sb[k];
+
     uint32_t vw[4][C::VW];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -350,15 +372,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
           for (int k = 0; k < C::VW; ++k) vw[u][k] = (VF == INT8) ? 0x80808080u : 0u;
         }
     }
-
-    // ---- S^T = K q^T
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < C::KSTEPS; ++j) {
-      uint32_t a0, a1, a2, a3;
-      k_frag<KF, C::KW>(kw, j, a0, a1, a2, a3);
-      mma16816(sacc, a0, a1, a2, a3, qf[j][0], qf[j][1]);
-    }
     const uint8_t* meta = st + C::K_BYTES + C::V_BYTES;
     float sl[4];
     if constexpr (!is_asym(KF)) {
@@ -384,14 +397,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
     if (!ok0) sl[0] = sl[1] = -INFINITY;
     if (!ok1) sl[2] = sl[3] = -INFINITY;
 
-    // ---- online softmax (log2 domain), lazy rescale
+    // ---- online softmax (log2 domain), lazy rescale: the running maximum m is
+    // only raised (with a reduction over the tile) when some logit exceeds it
+    // by more than 8, so probabilities stay <= 2^8 and most tiles skip it
     float mx0 = fmaxf(sl[0], sl[2]), mx1 = fmaxf(sl[1], sl[3]);
-#pragma unroll
-    for (int o = 4; o <= 16; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
     if (__any_sync(0xffffffffu, (mx0 > m0 + 8.0f) || (mx1 > m1 + 8.0f))) {
+#pragma unroll
+      for (int o = 4; o <= 16; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
       const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
       const float al0 = fast_exp2(m0 - n0), al1 = fast_exp2(m1 - n1);
       m0 = n0;
@@ -444,8 +459,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
     }
     __syncwarp();
     const int nx = it + C::STAGES - 1;
-    if (nx < my_tiles) issue(nx, nx % C::STAGES);
+    if (nx < my_tiles) issue(nx, stage == 0 ? C::STAGES - 1 : stage - 1);
     cp_async_commit();
+    stage = stage + 1 == C::STAGES ? 0 : stage + 1;
   }
   cp_async_wait<0>();
 
@@ -506,61 +522,82 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 3)
       }
     }
   }
-  if constexpr (KVARN) {
-    if (direct) {
+  if (direct) {
+    if constexpr (KVARN) {
       __syncthreads();
       for (int n = warp; n < G; n += kDecodeWarps) rotate_row_warp<D, true>(cRes + n * D, a.signs, a.cR, lane);
       __syncthreads();
       for (int i = threadIdx.x; i < G * D; i += blockDim.x) a.out[out_row0 * D + i] = f2bf(cRes[i]);
     }
-  }
-}
-
-// Log-sum-exp combine of the partitions of one (sequence, query head).
-template <int D, bool KVARN>
-__global__ void __launch_bounds__(256) decode_reduce_kernel(const DecodeArgs a) {
-  constexpr int NG = 256 / D;
-  __shared__ float s_acc[NG][D];
-  __shared__ float s_l[NG];
-  const int hq = blockIdx.x, s = blockIdx.y;
-  const int d = threadIdx.x % D, grp = threadIdx.x / D;
-  const int ctx = min(max(a.context_lens[s], 0), a.max_context_len);
-  uint16_t* o = a.out + (static_cast<size_t>(s) * a.num_q_heads + hq) * D;
-  if (ctx <= 0) {
-    if (grp == 0) o[d] = 0;
     return;
   }
-  const int np = (ctx + a.partition_tokens - 1) / a.partition_tokens;
-  const size_t r0 = (static_cast<size_t>(s) * a.num_q_heads + hq) * a.num_partitions;
-  const float* ml = a.ws_ml + 2 * r0;
-  const float* acc = a.ws_acc + r0 * D;
-  float M = -INFINITY;
-  for (int i = 0; i < np; ++i) M = fmaxf(M, ml[2 * i]);
-  float sa = 0.f, sl = 0.f;
-#pragma unroll 4
-  for (int i = grp; i < np; i += NG) {
-    const float w = fast_exp2(ml[2 * i] - M);
-    sa += w * acc[static_cast<size_t>(i) * D + d];
-    sl += w * ml[2 * i + 1];
-  }
-  s_acc[grp][d] = sa;
-  if (d == 0) s_l[grp] = sl;
+
+  // ---- the last CTA to finish a (sequence, kv-head) merges its partitions
+  __threadfence();
   __syncthreads();
-  if (grp == 0) {
-    float ta = 0.f, tl = 0.f;
+  int* s_last = reinterpret_cast<int*>(smem + C::MAIN);  // block ids are dead by now
+  const int np_s = (ctx + P - 1) / P;
+  if (threadIdx.x == 0) {
+    unsigned long long* ctr = a.counters + static_cast<size_t>(s) * Hkv + h;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), assumed, nv = 0;
+    int tries = 0;
+    do {  // counters carry the call's epoch: stale contents from any earlier use are reset
+      assumed = old;
+      nv = ((assumed >> 16) == a.epoch) ? assumed + 1 : ((a.epoch << 16) | 1ull);
+      old = atomicCAS(ctr, assumed, nv);
+    } while (old != assumed && ++tries < (1 << 20));
+    if (old != assumed) raise_error(8u);  // KVQ_DEVERR_COMBINE
+    s_last[0] = (old == assumed) && static_cast<int>(nv & 0xFFFFull) == np_s;
+  }
+  __syncthreads();
+  if (!s_last[0]) return;
+  __threadfence();
+  float* sW = reinterpret_cast<float*>(smem);  // [8][np_s] partition weights
+  float* sLinv = sW + 8 * kMaxPartitions;      // [8]
+  float* sRes = sLinv + 8;                     // [8][D]
+  for (int n = warp; n < G; n += kDecodeWarps) {
+    const size_t r0 = (out_row0 + n) * a.num_partitions;
+    float M = -INFINITY;
+    for (int q = lane; q < np_s; q += 32) M = fmaxf(M, __ldcg(a.ws_ml + 2 * (r0 + q)));
 #pragma unroll
-    for (int k = 0; k < NG; ++k) {
-      ta += s_acc[k][d];
-      tl += s_l[k];
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int q = lane; q < np_s; q += 32) {
+      const float w = fast_exp2(__ldcg(a.ws_ml + 2 * (r0 + q)) - M);
+      sW[n * np_s + q] = w;
+      L += w * __ldcg(a.ws_ml + 2 * (r0 + q) + 1);
     }
-    s_acc[0][d] = ta / tl;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) sLinv[n] = 1.0f / L;
   }
   __syncthreads();
-  if constexpr (KVARN) {
-    if (threadIdx.x < 32) rotate_row_warp<D, true>(&s_acc[0][0], a.signs, a.cR, threadIdx.x);
-    __syncthreads();
+  for (int i = threadIdx.x; i < G * (D / 4); i += blockDim.x) {
+    const int n = i / (D / 4), d4 = (i % (D / 4)) * 4;
+    const float4* src = reinterpret_cast<const float4*>(a.ws_acc + (out_row0 + n) * a.num_partitions * D + d4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int q = 0; q < np_s; ++q) {
+      const float4 v = __ldcg(src + static_cast<size_t>(q) * (D / 4));
+      const float w = sW[n * np_s + q];
+      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    }
+    const float li = sLinv[n];
+    if constexpr (KVARN) {
+      sRes[n * D + d4 + 0] = acc.x * li; sRes[n * D + d4 + 1] = acc.y * li;
+      sRes[n * D + d4 + 2] = acc.z * li; sRes[n * D + d4 + 3] = acc.w * li;
+    } else {
+      uint16_t* o = a.out + (out_row0 + n) * D + d4;
+      o[0] = f2bf(acc.x * li); o[1] = f2bf(acc.y * li);
+      o[2] = f2bf(acc.z * li); o[3] = f2bf(acc.w * li);
+    }
   }
-  if (grp == 0) o[d] = f2bf(s_acc[0][d]);
+  if constexpr (KVARN) {
+    __syncthreads();
+    for (int n = warp; n < G; n += kDecodeWarps) rotate_row_warp<D, true>(sRes + n * D, a.signs, a.cR, lane);
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) a.out[out_row0 * D + i] = f2bf(sRes[i]);
+  }
 }
 
 }  // namespace kvq

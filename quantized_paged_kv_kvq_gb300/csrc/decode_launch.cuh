@@ -1,5 +1,5 @@
-// Launch of the decode partition kernel (+ the log-sum-exp combine when a
-// sequence spans several partitions) for one template instance.
+// Launch of the decode kernel for one template instance (one launch: the last
+// CTA of each (sequence, kv-head) merges its partitions).
 #pragma once
 
 #include <atomic>
@@ -22,17 +22,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
-  if (a.phase & 1) {
-    const dim3 grid(a.num_kv_heads, a.num_seqs, a.num_partitions);
-    kern<<<grid, kDecodeWarps * 32, C::SMEM, st>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  if ((a.phase & 2) && a.num_partitions > 1) {
-    decode_reduce_kernel<D, KVARN><<<dim3(a.num_q_heads, a.num_seqs), 256, 0, st>>>(a);
-    e = cudaGetLastError();
-  }
-  return e;
+  const dim3 grid(a.num_kv_heads, a.num_seqs, a.num_partitions);
+  kern<<<grid, kDecodeWarps * 32, C::SMEM, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace kvq

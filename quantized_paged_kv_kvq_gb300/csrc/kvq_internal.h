@@ -9,6 +9,8 @@ namespace kvq {
 
 // Longest split-K context partition (tokens); bounds the block-id staging area.
 constexpr int kMaxPartition = 8192;
+// Most split-K partitions per sequence (bounds the merge's shared memory).
+constexpr int kMaxPartitions = 512;
 
 struct WriteArgs {
   const uint16_t* key;    // bf16 bits
@@ -42,11 +44,14 @@ struct DecodeArgs {
   const int8_t* signs;
   float* ws_acc;  // [S, Hq, NP, D]
   float* ws_ml;   // [S, Hq, NP, 2]
+  unsigned long long* counters;  // [S, Hkv]: (epoch << 16) | partitions done
+  unsigned long long epoch;      // 48-bit tag of this call
   int num_seqs;
   int num_q_heads;
   int num_kv_heads;
   int gqa;
   int block_size;
+  int block_shift;  // log2(block_size)
   int num_blocks;
   int max_blocks_per_seq;
   int max_context_len;
@@ -55,7 +60,6 @@ struct DecodeArgs {
   float qk_scale;        // sm_scale * log2(e) [* k_scale for symmetric K]
   float v_scale;         // symmetric V: multiplies the output
   float cR;
-  int phase;  // bit 0: partition kernel, bit 1: log-sum-exp combine
 };
 
 cudaError_t launch_write(const WriteArgs& a, int head_dim, int kf, int vf, bool kvarn,

@@ -25,6 +25,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARGUMENT", 2: "KVQ_ERR_UNSUPPORTED",
 DEVERR_SLOT_RANGE = 1
 DEVERR_BLOCK_RANGE = 2
 DEVERR_CONTEXT_RANGE = 4
+DEVERR_COMBINE = 8
 
 
 class KvqError(RuntimeError):
@@ -55,10 +56,6 @@ SIGNATURES = {
                                 _SZ, _P]),
     "kvq_paged_decode_ex": (_I32, [_DESC, _P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _I32, _F32,
                                    _I32, _P, _SZ, _P]),
-    "kvq_paged_decode_partitions": (_I32, [_DESC, _P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _I32,
-                                           _F32, _I32, _P, _SZ, _P]),
-    "kvq_paged_decode_combine": (_I32, [_DESC, _P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _I32,
-                                        _F32, _I32, _P, _SZ, _P]),
     "kvq_paged_decode_static": (_I32, [_DESC, _P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _I32,
                                        _F32, _I32, _P]),
     "kvq_paged_decode_static_capacity": (_SZ, []),
@@ -224,22 +221,6 @@ def kvq_paged_decode(cache: KVCache, query: torch.Tensor, out: torch.Tensor,
     """out[s, h] = softmax(sm_scale q k^T) v over the paged cache (bf16 [S, Hq, D])."""
     return _decode_call("kvq_paged_decode_ex", cache, query, out, block_table, context_lens,
                         max_context_len, sm_scale, workspace, partition_tokens, stream)
-
-
-def kvq_paged_decode_partitions(cache, query, out, block_table, context_lens, max_context_len,
-                                sm_scale, workspace=None, partition_tokens=0, stream=None):
-    """First launch of kvq_paged_decode (per-partition attention)."""
-    return _decode_call("kvq_paged_decode_partitions", cache, query, out, block_table,
-                        context_lens, max_context_len, sm_scale, workspace, partition_tokens,
-                        stream)
-
-
-def kvq_paged_decode_combine(cache, query, out, block_table, context_lens, max_context_len,
-                             sm_scale, workspace=None, partition_tokens=0, stream=None):
-    """Second launch of kvq_paged_decode (log-sum-exp combine of partitions)."""
-    return _decode_call("kvq_paged_decode_combine", cache, query, out, block_table,
-                        context_lens, max_context_len, sm_scale, workspace, partition_tokens,
-                        stream)
 
 
 def kvq_paged_decode_static(cache: KVCache, query: torch.Tensor, out: torch.Tensor,

@@ -106,7 +106,7 @@ def test_decode_validation(lib):
     n = ctypes.c_size_t(0)
     assert lib.kvq_decode_workspace_size_ex(ctypes.byref(d), 4, 32, 1024, 256,
                                             ctypes.byref(n)) == 0
-    assert n.value == 4 * 32 * 4 * (128 + 2) * 4
+    assert n.value == 4 * 32 * 4 * (128 + 2) * 4 + 4 * 8 * 8  # partials + counters
     assert lib.kvq_decode_workspace_size_ex(ctypes.byref(d), 4, 32, 200, 256,
                                             ctypes.byref(n)) == 0
     assert n.value == 0  # one partition: no workspace
