@@ -45,7 +45,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    p.add_argument("--partition", type=int, default=0, help="decode partition tokens (0 = auto)")
+    p.add_argument("--ctas", type=int, default=0, help="decode CTAs per kv-head group (0 = auto)")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -354,7 +354,7 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
                                scale(value, wl.v_scale_rule), wl.kvarn, signs, device=dev)
     out = torch.empty_like(query)
     sm_scale = float(np.float32(1.0 / np.sqrt(wl.head_dim)))
-    P = args.partition
+    P = args.ctas
     ws_bytes = kvq.kvq_decode_workspace_size(cache, wl.num_seqs, wl.num_q_heads,
                                              wl.max_context_len, P)
     ws = torch.empty(max(ws_bytes, 16) // 4 + 4, dtype=torch.float32, device=dev)
@@ -465,7 +465,7 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
                    "head_dim": wl.head_dim, "block_size": wl.block_size,
                    "k_fmt": wl.k_fmt, "v_fmt": wl.v_fmt, "kvarn": wl.kvarn,
                    "context_tokens": int(wl.context_lens.sum()),
-                   "partition_tokens": P or "auto", "l2": "flushed before the write and before the decode (2xL2 memset, "
+                   "decode_ctas": P or "auto", "l2": "flushed before the write and before the decode (2xL2 memset, "
                    "then a 2xL2 read), outside the timed events"},
         "decode_tok_s": world * wl.num_seqs * K / t_dec,
         "decode_us": 1e6 * t_dec / K, "decode_partitions": ws_bytes > 0,

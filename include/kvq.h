@@ -128,8 +128,11 @@ kvq_status kvq_write_cache(const kvq_cache_desc* cache, void* k_cache, void* v_c
 
 /*
  * kvq_decode_workspace_size -- bytes of device workspace kvq_paged_decode
- * needs for these sizes (0 when one context partition suffices).  Depends on
- * the device's SM count (current device).
+ * needs for these sizes: partial results of sequences split between CTAs
+ * (num_ctas * 2 * num_q_heads * (head_dim + 2) * 4 bytes, 0 with one CTA)
+ * two 8-byte completion tags per (CTA, group of 8 kv-heads) and one 8-byte
+ * merge claim per (sequence, group of 8 kv-heads).  Depends on the device's
+ * SM count (current device).
  */
 kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_seqs,
                                      int32_t num_q_heads, int32_t max_context_len,
@@ -139,8 +142,10 @@ kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_se
  * kvq_paged_decode -- one new query token per sequence attends to its paged,
  * quantized context (issue #4025 'methods' item 3; PR #4893 side note).
  *
- * query: device bf16 [num_seqs, num_q_heads, head_dim], contiguous.
- * out:   device bf16 [num_seqs, num_q_heads, head_dim], contiguous.
+ * query: device bf16 [num_seqs, num_q_heads, head_dim], contiguous, 16-byte
+ *   aligned.
+ * out:   device bf16 [num_seqs, num_q_heads, head_dim], contiguous, 16-byte
+ *   aligned.
  *   q-head h reads kv-head h / (num_q_heads / num_kv_heads); the ratio must be
  *   an integer <= 8.
  * block_table: device int32 [num_seqs, max_blocks_per_seq]; entries past
@@ -151,10 +156,13 @@ kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_se
  * sm_scale: logits are sm_scale * <q, k>.
  * workspace: device memory of >= kvq_decode_workspace_size(...) bytes
  *   (may be NULL when that size is 0), 16-byte aligned; its contents on entry
- *   do not matter (completion counters inside it carry a per-call tag).  Two
+ *   do not matter (its completion tags and claims carry a per-call value).  Two
  *   calls that overlap on the GPU must not share a workspace.
- * One kernel launch: CTAs of (kv-head, sequence, context partition); the last
- *   CTA to finish a (sequence, kv-head) merges its partitions (log-sum-exp).
+ * One kernel launch, stream-K: each CTA owns an equal contiguous range of the
+ *   16-token tiles of all sequences (for a group of up to 8 kv-heads).  A
+ *   sequence split between CTAs leaves partial results that are merged
+ *   (log-sum-exp) by a CTA that, after its own range, finds every other part
+ *   published.  Results do not depend on the split beyond rounding.
  * out[s, h] = sum_t softmax_t(sm_scale <q, k_t>) v_t over the dequantized
  *   cache, computed with fp32 softmax and fp32 accumulation (keys and values
  *   enter the tensor cores as exact fp16 code values; the query is rounded to
@@ -168,21 +176,20 @@ kvq_status kvq_paged_decode(const kvq_cache_desc* cache, const void* k_cache,
                             size_t workspace_bytes, kvq_stream_t stream);
 
 /*
- * kvq_paged_decode_ex -- kvq_paged_decode with an explicit context
- * partition size (tokens per split-K partition, a multiple of 64, at most
- * 8192; 0 = the automatic choice); sizes that need more than 512 partitions
- * per sequence return KVQ_ERR_UNSUPPORTED.  The workspace must hold
- * kvq_decode_workspace_size_ex(...) bytes for the same partition size.
+ * kvq_paged_decode_ex -- kvq_paged_decode with an explicit number of CTAs
+ * per group of 8 kv-heads (the stream-K ranges the tiles are split into,
+ * 1..65535; 0 = the automatic choice: two per SM).  The workspace must hold
+ * kvq_decode_workspace_size_ex(...) bytes for the same num_ctas.
  */
 kvq_status kvq_decode_workspace_size_ex(const kvq_cache_desc* cache, int32_t num_seqs,
                                         int32_t num_q_heads, int32_t max_context_len,
-                                        int32_t partition_tokens, size_t* bytes);
+                                        int32_t num_ctas, size_t* bytes);
 kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
                                const void* v_cache, void* out, const void* query,
                                int32_t num_seqs, int32_t num_q_heads,
                                const int32_t* block_table, int32_t max_blocks_per_seq,
                                const int32_t* context_lens, int32_t max_context_len,
-                               float sm_scale, int32_t partition_tokens, void* workspace,
+                               float sm_scale, int32_t num_ctas, void* workspace,
                                size_t workspace_bytes, kvq_stream_t stream);
 
 /*
@@ -211,14 +218,14 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
  * reads is written earlier in the same call), but two calls whose kernels
  * overlap on the GPU (different streams, or several host threads) race on it
  * and corrupt each other's results -- serialize them.
- * Arguments and results are those of kvq_paged_decode_ex.
+ * Arguments and results are those of kvq_paged_decode_ex (num_ctas included).
  */
 kvq_status kvq_paged_decode_static(const kvq_cache_desc* cache, const void* k_cache,
                                    const void* v_cache, void* out, const void* query,
                                    int32_t num_seqs, int32_t num_q_heads,
                                    const int32_t* block_table, int32_t max_blocks_per_seq,
                                    const int32_t* context_lens, int32_t max_context_len,
-                                   float sm_scale, int32_t partition_tokens, kvq_stream_t stream);
+                                   float sm_scale, int32_t num_ctas, kvq_stream_t stream);
 /* Bytes of the scratch array kvq_paged_decode_static uses. */
 size_t kvq_paged_decode_static_capacity(void);
 
@@ -250,7 +257,8 @@ kvq_status kvq_calibrate_scale(const void* x, int64_t n, float qmax, float* scal
 #define KVQ_DEVERR_SLOT_RANGE 1u  /* a slot id past num_blocks*block_size */
 #define KVQ_DEVERR_BLOCK_RANGE 2u /* a block-table entry outside [0, num_blocks) */
 #define KVQ_DEVERR_CONTEXT_RANGE 4u /* a context length outside [0, max_context_len] */
-#define KVQ_DEVERR_COMBINE 8u       /* a partition-merge counter update gave up */
+#define KVQ_DEVERR_COMBINE 8u       /* a split-sequence merge counter update gave up */
+#define KVQ_DEVERR_TIMEOUT 16u      /* a pipeline barrier wait gave up (results invalid) */
 
 /*
  * kvq_get_device_error -- synchronizes `stream`, then reads and clears the

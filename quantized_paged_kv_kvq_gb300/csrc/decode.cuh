@@ -7,41 +7,51 @@
 // decode through the same paged-attention kernel.
 //
 // Design (one GPU, HBM-bound):
-//  * grid (kv-head, sequence, context partition); a CTA of kWarps warps owns
-//    one (sequence, kv-head, partition of P tokens) and its G query heads;
-//    each warp streams every kWarps-th 16-token tile of the partition through
-//    its own cp.async ring in shared memory (lane-linear, bank-conflict
-//    free), so no block-wide barrier sits in the token loop;
+//  * stream-K: grid (ranges, kv-head groups of <= 8 heads); the 16-token
+//    tiles of all sequences, in order, are cut into equal contiguous ranges,
+//    one per CTA, so every SM gets the same work whatever the context lengths;
+//    one consumer warp per kv-head.  Each tile is one pipeline stage: a TMA
+//    box per kv-head for K and V (cp.async.bulk.tensor, 128B/64B swizzle) plus
+//    one box per metadata array, completing on the stage's "full" mbarrier;
+//    warps copy the stage into registers, release it on its "empty" mbarrier
+//    and one elected thread refills it at once.  A block's rows of all heads
+//    stream from HBM back to back.
 //  * codes become exact fp16 values in registers (byte permutes / nibble
 //    masks onto the 1024.0 exponent, or the native e4m3 convert) and feed
 //    mma.sync m16n8k16 with fp32 accumulation: S^T = K q^T with 16 tokens x
 //    8 query heads, then O^T += V^T P^T with 16 dims x 8 heads -- the GQA
-//    group is the n = 8 dimension (G = 4 pads it with zero queries);
-//  * the dot-product dimension is permuted so that every lane's operands
-//    come from contiguous 16-byte loads; the query is permuted to match;
-//  * online softmax in the log2 domain, rescaling only when the running
-//    maximum grows by more than 2^8; scales, zero points and sigma are folded
-//    in after the k-sum (K) or into the probabilities (V);
-//  * partitions are combined in shared memory across warps and, when a
-//    sequence spans several partitions, by a second log-sum-exp kernel.
+//    group is the n = 8 dimension (G = 4 pads it with zero queries).  The
+//    operands come from shared memory with 16-byte loads; the dot-product
+//    dimension is permuted so each lane's slice is contiguous (the query is
+//    permuted to match) and tokens are assigned to mma rows so that, with the
+//    swizzle, every 16-byte load of a quarter-warp hits distinct banks.
+//  * online softmax in the log2 domain; the running maximum is raised (with
+//    a reduction) only when a logit exceeds it by more than 8, so P <= 2^8;
+//    scales, zero points and sigma are folded in after the k-sum (K) or into
+//    the probabilities (V).
+//  * a sequence split between ranges is merged (log-sum-exp) by the last CTA
+//    to finish its part, from L2, inside the same launch.
 #pragma once
+
+#include <cuda.h>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
 
-constexpr int kDecodeWarps = 4;
-constexpr int kDecodeMinBlocks = 4;  // resident CTAs per SM the register budget targets
+constexpr int kHeadsPerCta = 8;  // kv-heads (= consumer warps) per CTA
+constexpr int kSpinLimit = 1 << 26;  // polls of an mbarrier before giving up
 
-template <int D, int KF, int VF, bool KVARN>
+template <int D_, int KF, int VF, bool KVARN>
 struct DecodeCfg {
+  static constexpr int D = D_;
   static constexpr int KB = row_bytes(KF, D);
   static constexpr int VB = row_bytes(VF, D);
   static constexpr int KSTEPS = D / 16;
   static constexpr int DTILES = D / 16;
   static constexpr int K_LANE = KB / 4;                  // K bytes per row per lane
-  static constexpr int KPS = K_LANE < 16 ? K_LANE : 16;  // cp.async piece
+  static constexpr int KPS = K_LANE < 16 ? K_LANE : 16;  // load piece
   static constexpr int KP = K_LANE / KPS;                // pieces per row
   static constexpr int KSTRIDE_P = KB / KP;              // bytes between pieces
   static constexpr int KW = K_LANE / 4;                  // words per row per lane
@@ -49,22 +59,45 @@ struct DecodeCfg {
   static constexpr int VW = VPS / 4;
   static constexpr int KMF = is_asym(KF) ? (KVARN ? 3 : 2) : 0;
   static constexpr int VMF = is_asym(VF) ? (KVARN ? 3 : 2) : 0;
-  static constexpr int K_BYTES = 2 * KP * 32 * KPS;
-  static constexpr int V_BYTES = 4 * 32 * VPS;
-  static constexpr int M_BYTES = (KMF + VMF) * 32;
-  static constexpr int STAGE = K_BYTES + V_BYTES + M_BYTES;
-  static constexpr int STAGES = STAGE >= 4096 ? 3 : STAGE >= 3072 ? 4 : STAGE >= 2048 ? 5 : 8;
-  static constexpr int WARP_SMEM = STAGES * STAGE;
-  static constexpr int RING = kDecodeWarps * WARP_SMEM;
-  static constexpr int COMBINE = kDecodeWarps * 8 * (D + 2) * 4 + 8 * D * 4;  // warps
-  static constexpr int MERGE = (8 * kMaxPartitions + 8 + 8 * D) * 4;        // partitions
-  static constexpr int QAREA = 8 * D * 4;
-  static constexpr int max2(int x, int y) { return x > y ? x : y; }
-  // rings and the query rows live side by side; the combines reuse it all later
-  static constexpr int MAIN = max2(RING + QAREA, max2(COMBINE, MERGE));
-  static constexpr int SMEM = MAIN + (kMaxPartition / 16) * 4;
+  static constexpr int K_HEAD = 16 * KB;  // bytes of one head's 16-token box
+  static constexpr int V_HEAD = 16 * VB;
+  // swizzle of the TMA boxes: 16-byte chunk index ^= address bits [7, 7+n)
+  static constexpr int swz_bits(int rb) { return rb == 128 ? 3 : rb == 64 ? 2 : 0; }
+  static constexpr int K_SWZ = swz_bits(KB);
+  static constexpr int V_SWZ = swz_bits(VB);
+  static constexpr int align(int x) { return (x + 1023) / 1024 * 1024; }
+  static constexpr int align128(int x) { return (x + 127) / 128 * 128; }
+  static constexpr int stage_bytes(int hpc) {
+    return align(hpc * K_HEAD) + align(hpc * V_HEAD) + align(align128(hpc * KMF * 32) + hpc * VMF * 32);
+  }
+  static constexpr int STAGE_MAX = stage_bytes(kHeadsPerCta);
+  static constexpr int STAGES = STAGE_MAX >= 24576 ? 3 : STAGE_MAX >= 16384 ? 5 : 6;
+  static constexpr bool KVARN_ = KVARN;
   static_assert(KW * 4 == K_LANE && VW * 4 == VPS, "layout");
 };
+
+// Shared memory of a CTA (bytes): the ring; per warp its query rows (G rows of
+// D bf16, filled ahead of each segment) and, with KVarN, a float row for the
+// query rotation; per stage a tile header and two mbarriers; a scratch area
+// with the producer's cursor; and 1 KB of alignment.
+__host__ __device__ constexpr int q_rows_bytes(int g, int d) { return (g * d * 2 + 15) / 16 * 16; }
+template <class C>
+__host__ __device__ constexpr int decode_smem_bytes(int hpc, int g) {
+  return C::STAGES * C::stage_bytes(hpc) + hpc * q_rows_bytes(g, C::D) + (C::KVARN_ ? hpc * C::D * 4 : 0) +
+         C::STAGES * 48 + 192 + 1024;
+}
+
+// Row of mma row r (0..15) of a tile: the QK row r holds token kRow[r].  With
+// V's k-slot tokens kRow[c + 8(u&1) + 4(u>>1)] this makes each quarter-warp's
+// 16-byte shared loads conflict-free under the swizzle and lets lane (g, c)
+// take its P operand from lanes c and c + 4.
+__device__ __forceinline__ int tile_row(int r) {
+  // 0,5,2,7, 8,13,10,15, 4,1,6,3, 12,9,14,11
+  const int lo = r & 3, hi = (r >> 2) & 1, top = r >> 3;
+  const int odd = lo & 1;
+  return lo + 8 * hi + 4 * (odd ^ top);
+}
+__device__ __forceinline__ int v_token(int c, int u) { return tile_row(c + 8 * (u & 1) + 4 * (u >> 1)); }
 
 // d index of the query element that meets k-slot (2c, 2c+1, 2c+8, 2c+9)[e]
 // of k-step j in lane-quad position c.
@@ -82,7 +115,7 @@ __device__ __forceinline__ int kslot_d(int c, int j, int e) {
   }
 }
 
-// K operand (rows = tokens 2g, 2g+1; 4 k-slots per lane) for k-step j.
+// K operand (rows = the lane's two tokens; 4 k-slots per lane) for k-step j.
 template <int KF, int KW>
 __device__ __forceinline__ void k_frag(const uint32_t (&kw)[2][KW], int j, uint32_t& a0,
                                        uint32_t& a1, uint32_t& a2, uint32_t& a3) {
@@ -111,7 +144,7 @@ __device__ __forceinline__ void k_frag(const uint32_t (&kw)[2][KW], int j, uint3
   }
 }
 
-// V operand (rows = dims, k = tokens 4c..4c+3) for d-tile i; exact code values.
+// V operand (rows = dims, k = the lane's 4 tokens) for d-tile i; exact values.
 template <int VF>
 __device__ __forceinline__ void v_pair(uint32_t wa, uint32_t wb, int i, uint32_t& rg,
                                        uint32_t& rg8) {
@@ -170,6 +203,7 @@ __device__ __forceinline__ void rotate_row_warp(float* row, const int8_t* signs,
   __syncwarp();
 #pragma unroll
   for (int e = 0; e < E; ++e) row[lane * E + e] = v[e];
+  __syncwarp();
 }
 
 __device__ __forceinline__ uint16_t f2bf(float x) {
@@ -177,225 +211,744 @@ __device__ __forceinline__ uint16_t f2bf(float x) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// ---------------------------------------------------------------------------
+// mbarrier / TMA primitives
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for `parity` of an mbarrier, at most kSpinLimit polls; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int n = 0; n < kSpinLimit; ++n)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+// Shared address of 16-byte chunk `chunk` (plus `byte` within it) of row `row`
+// of a swizzled box starting at `base` (1024-byte aligned for swizzled boxes).
+template <int RB, int SWZ>
+__device__ __forceinline__ uint32_t swz_addr(uint32_t base, int row, int chunk, int byte = 0) {
+  const uint32_t off = static_cast<uint32_t>(row * RB + chunk * 16);
+  const uint32_t phys = SWZ ? (off ^ (((off >> 7) & ((1u << SWZ) - 1)) << 4)) : off;
+  return base + phys + byte;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+  return r;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 r;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
+  return r;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a));
+  return r;
+}
+__device__ __forceinline__ float lds_half(uint32_t a) {
+  uint16_t r;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
+  return __half2float(__ushort_as_half(r));
+}
+
+
+// Walsh-Hadamard butterfly over rows of D = 8 * E values where lane (g, c) of
+// a warp holds the E consecutive values g*E .. g*E+E-1 of row c (the layout of
+// the PV accumulators); same stage order as fwht_lanes.
+template <int E>
+__device__ __forceinline__ void fwht_accum_rows(float (&v)[E], int g) {
+#pragma unroll
+  for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      if ((i & h) == 0) {
+        float x = v[i], y = v[i + h];
+        v[i] = __fadd_rn(x, y);
+        v[i + h] = __fsub_rn(x, y);
+      }
+    }
+  }
+#pragma unroll
+  for (int gm = 1; gm < 8; gm <<= 1) {
+    const bool upper = (g & gm) != 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const float other = __shfl_xor_sync(0xffffffffu, v[i], 4 * gm);
+      v[i] = upper ? __fsub_rn(other, v[i]) : __fadd_rn(v[i], other);
+    }
+  }
+}
+
+// mma16816 with the accumulator given as four separate floats
+__device__ __forceinline__ void mma16816(float& c0, float& c1, float& c2, float& c3, uint32_t a0,
+                                         uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The producer's position in the range.
+struct Cursor {
+  long long ps;  // global index of the first tile of sequence s
+  int s, t;      // sequence and tile of the next load
+  int tiles, ctx;
+  int blk;         // block id of that tile (read ahead)
+  int nx, nx_ctx;  // next sequence of the range with tokens (num_seqs: none)
+  int i;           // loads issued
+};
+
+struct DecodeMaps {
+  CUtensorMap k, v, km, vm;
+};
+
+// One stage's tile: which sequence / tile it is and how it ends a segment.
+struct TileHeader {
+  int s;       // sequence
+  int t;       // 16-token tile index within the sequence
+  int valid;   // valid tokens in the tile (1..16)
+  int flags;   // bit 0: first tile of this CTA's segment of s; bit 1: last tile
+  int ps;      // global index of the sequence's first tile
+  int tiles;   // tiles of the sequence
+  int next_s;  // sequence of the range's next segment (first tiles only), or -1
+  int pad;
+};
+
+__device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
+  uint16_t r;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
+  return r;
+}
+__device__ __forceinline__ void bar_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int s) {
+  const int ctx = a.context_lens[s];
+  return ctx <= 0 ? 0 : (min(ctx, a.max_context_len) + 15) >> 4;
+}
+
+// First global tile of stream-K range k (range NC starts at T).  Ranges are cut
+// in proportion to weights: split_wa for the first split_h ranges, split_wb
+// for the rest.
+__device__ __forceinline__ long long range_start(const DecodeArgs& a, long long T, int k) {
+  const long long wk = static_cast<long long>(a.split_wa) * min(k, a.split_h) +
+                       static_cast<long long>(a.split_wb) * max(k - a.split_h, 0);
+  const long long wt = static_cast<long long>(a.split_wa) * a.split_h +
+                       static_cast<long long>(a.split_wb) * (a.num_ctas - a.split_h);
+  return T * wk / wt;
+}
+// The range holding global tile x < T: the largest k with range_start(k) <= x.
+__device__ __forceinline__ int range_of(const DecodeArgs& a, long long x, long long T) {
+  int lo = 0, hi = a.num_ctas - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (range_start(a, T, mid) <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int N>
+__device__ __forceinline__ void store_bf16_run(uint16_t* dst, const float (&v)[N]) {
+  static_assert(N % 8 == 0, "run of 16-byte pieces");
+#pragma unroll
+  for (int i = 0; i < N / 8; ++i) {
+    uint4 w;
+    w.x = static_cast<uint32_t>(f2bf(v[8 * i])) | (static_cast<uint32_t>(f2bf(v[8 * i + 1])) << 16);
+    w.y = static_cast<uint32_t>(f2bf(v[8 * i + 2])) | (static_cast<uint32_t>(f2bf(v[8 * i + 3])) << 16);
+    w.z = static_cast<uint32_t>(f2bf(v[8 * i + 4])) | (static_cast<uint32_t>(f2bf(v[8 * i + 5])) << 16);
+    w.w = static_cast<uint32_t>(f2bf(v[8 * i + 6])) | (static_cast<uint32_t>(f2bf(v[8 * i + 7])) << 16);
+    reinterpret_cast<uint4*>(dst)[i] = w;
+  }
+}
+template <int N>
+__device__ __forceinline__ void store_f32_run(float* dst, const float (&v)[N]) {
+  static_assert(N % 4 == 0, "run of 16-byte pieces");
+#pragma unroll
+  for (int i = 0; i < N / 4; ++i)
+    reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+template <int N>
+__device__ __forceinline__ void ldcg_vec(const float* p, float (&v)[N]) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(p) + i);
+      v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+    }
+  } else {
+    static_assert(N == 2, "vector width");
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(p));
+    v[0] = x.x; v[1] = x.y;
+  }
+}
+
+// Log-sum-exp merge of the partial results of sequence s (tiles [ps, ps+tiles)
+// of the global order) held in the slots of stream-K ranges ka..kb, by one warp
+// for its kv-head's G query heads, four at a time: lane (nn, r) owns query head
+// nn's dims r*DL .. r*DL+DL-1.  Every lane reads every range's (m, l) itself;
+// the loads of PU ranges are issued together and merged with a running
+// maximum, so a merge costs a few L2 round trips whatever the number of ranges.
+template <int D, bool KVARN>
+__device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long long ps, int tiles,
+                                               long long T, int NC, int HG, int hg, int warp,
+                                               int lane, int hpc) {
+  constexpr int LQ = 8;                     // lanes per query head
+  constexpr int DL = D / LQ;                // dims per lane
+  constexpr int PU = 64 / DL < 8 ? 64 / DL : 8;  // ranges per batch of loads
+  const int G = a.gqa, rows = hpc * G;
+  const int r = lane % LQ;
+  const int ka = range_of(a, ps, T), kb = range_of(a, ps + tiles - 1, T);
+  const int np = kb - ka + 1;
+  const int h = hg * hpc + warp;
+#pragma unroll 1
+  for (int n0 = 0; n0 < G; n0 += 32 / LQ) {  // every lane runs every pass (shuffles below)
+    const int nn = n0 + lane / LQ;
+    const bool act = nn < G;
+    // slot row of range ka + p for query head nn, or -1 if the range is empty
+    auto slot_of = [&](int p) -> long long {
+      if (!act || p >= np) return -1;
+      const int kk = ka + p;
+      const long long r0 = range_start(a, T, kk), r1 = range_start(a, T, kk + 1);
+      if (r0 >= r1) return -1;
+      const int jj = (r0 >= ps) ? 0 : 1;
+      return ((static_cast<long long>(kk) * HG + hg) * 2 + jj) * rows + warp * G + nn;
+    };
+    float M = -INFINITY, Lsum = 0.f;
+    float acc[DL];
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[e] = 0.f;
+#pragma unroll 1
+    for (int p0 = 0; p0 < np; p0 += PU) {
+      float ml[PU][2], v[PU][DL];
+#pragma unroll
+      for (int u = 0; u < PU; ++u) {
+        const long long sl = slot_of(p0 + u);
+        if (sl >= 0) {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + 2 * sl));
+          ml[u][0] = x.x;
+          ml[u][1] = x.y;
+          ldcg_vec<DL>(a.ws_acc + sl * D + r * DL, v[u]);
+        } else {
+          ml[u][0] = -INFINITY;
+          ml[u][1] = 0.f;
+#pragma unroll
+          for (int e = 0; e < DL; ++e) v[u][e] = 0.f;
+        }
+      }
+      float bm = ml[0][0];
+#pragma unroll
+      for (int u = 1; u < PU; ++u) bm = fmaxf(bm, ml[u][0]);
+      if (bm > M) {  // raise the running maximum, rescaling what was summed so far
+        const float sc = fast_exp2(M - bm);
+        Lsum *= sc;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) acc[e] *= sc;
+        M = bm;
+      }
+#pragma unroll
+      for (int u = 0; u < PU; ++u) {
+        const float w = fast_exp2(ml[u][0] - M);
+        Lsum += w * ml[u][1];
+#pragma unroll
+        for (int e = 0; e < DL; ++e) acc[e] += w * v[u][e];
+      }
+    }
+    const float il = act ? 1.0f / Lsum : 0.f;
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[e] *= il;
+    if constexpr (KVARN) {  // inverse rotation x = d . (cR * H y) across the LQ lanes
+      fwht_lanes<DL, LQ>(acc, r);
+#pragma unroll
+      for (int e = 0; e < DL; ++e) {
+        const int dd = r * DL + e;
+        const float sgn = (a.signs != nullptr && a.signs[dd] < 0) ? -1.f : 1.f;
+        acc[e] = __fmul_rn(acc[e], a.cR) * sgn;
+      }
+    }
+    if (act) {
+      uint16_t* orow = a.out + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G + nn) * D + r * DL;
+#pragma unroll
+      for (int e = 0; e < DL; ++e) orow[e] = f2bf(acc[e]);
+    }
+  }
+}
+
+// Stream-K decode: CTA (k, hg) owns tiles [k*T/NC, (k+1)*T/NC) of the global
+// tile order (sequence-major, 16 tokens of all this group's heads per tile).
+// Thread 0 is also the producer that keeps the ring full.  A sequence the
+// range covers only in part leaves a partial result in the range's slot,
+// published with the call's tag by the group's last warp (the others never
+// wait for it); after its own range, a CTA that finds the tags of every other
+// range of such a sequence merges the slots.  Store-then-fence-then-load of
+// the tags guarantees at least one finder; a claim word per sequence keeps it
+// to one.
 template <int D, int KF, int VF, bool KVARN>
-__global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeMinBlocks)
-    decode_partition_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
+    decode_partition_kernel(const DecodeArgs a, const __grid_constant__ DecodeMaps maps) {
   using C = DecodeCfg<D, KF, VF, KVARN>;
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int h = blockIdx.x, s = blockIdx.y, p = blockIdx.z;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;  // the window is padded by 1 KB
+  uint8_t* smem = smem_raw + (base_s - raw_s);
+
+  const int k = blockIdx.x, NC = gridDim.x, hg = blockIdx.y, HG = gridDim.y;
+  const int hpc = a.heads_per_cta;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int G = a.gqa;
-  int ctx = a.context_lens[s];
-  if (ctx < 0 || ctx > a.max_context_len) {  // contract violation: clamp, flag
-    if (threadIdx.x == 0 && h == 0 && p == 0) raise_error(4u);  // KVQ_DEVERR_CONTEXT_RANGE
-    ctx = ctx < 0 ? 0 : a.max_context_len;
-  }
-  const int P = a.partition_tokens;
-  const int t_begin = p * P;
-  const bool direct = a.num_partitions == 1;
-  const size_t out_row0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G;
+  const int G = a.gqa, S = a.num_seqs;
+  const int h = hg * hpc + warp;  // this warp's kv-head
+  const int pub = hpc - 1;        // the warp that publishes partial results
+  const int stage_bytes = C::stage_bytes(hpc);
+  const int v_off = C::align(hpc * C::K_HEAD);
+  const int m_off = v_off + C::align(hpc * C::V_HEAD);  // K metadata box, then V's
+  const int vm_off = m_off + C::align128(hpc * C::KMF * 32);
+  const uint32_t ring_end = C::STAGES * stage_bytes;
+  const int qrb = q_rows_bytes(G, D);
+  const uint32_t qbuf_s = base_s + ring_end + warp * qrb;  // this warp's query rows (bf16)
+  const uint32_t rot_off = ring_end + hpc * qrb;           // KVarN: one float row per warp
+  const uint32_t hdr_off = rot_off + (KVARN ? hpc * D * 4 : 0);
+  TileHeader* hdr = reinterpret_cast<TileHeader*>(smem + hdr_off);
+  const uint32_t full_s = base_s + hdr_off + C::STAGES * sizeof(TileHeader);
+  const uint32_t empty_s = full_s + 8 * C::STAGES;
+  long long* scratch =
+      reinterpret_cast<long long*>(smem + hdr_off + C::STAGES * (sizeof(TileHeader) + 16));
+  // scratch: [0] T, [1] first sequence, [2] its first tile, [3] R1, [4..12) scan,
+  // [12..16) partial segments: (first tile, sequence << 32 | tiles) per end of the range
 
-  if (t_begin >= ctx) {
-    if (p == 0) {  // empty context: the output is zero
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x) a.out[out_row0 * D + i] = 0;
+  // this warp's G query rows of sequence s -> shared memory (asynchronous)
+  auto prefetch_q = [&](int s) {
+    const uint16_t* src =
+        a.query + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G) * D;
+    for (int i = lane; i < G * D / 8; i += 32) cp_async<16>(qbuf_s + 16 * i, src + 8 * i);
+    cp_async_commit();
+  };
+
+  // ---- context checks; zero outputs of the empty sequences this CTA owns
+  if (k == 0 && hg == 0) {
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+      const int ctx = a.context_lens[s];
+      if (ctx < 0 || ctx > a.max_context_len) raise_error(4u);  // KVQ_DEVERR_CONTEXT_RANGE
     }
-    return;
   }
-  const int len = min(ctx - t_begin, P);
-  const int ntiles = (len + 15) >> 4;
-  const int Hkv = a.num_kv_heads;
-  const int bs_shift = a.block_shift, bs_mask = a.block_size - 1;
+  for (int s = k; s < S; s += NC) {
+    if (seq_tiles(a, s) == 0) {
+      uint16_t* o = a.out + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G) * D;
+      for (int i = lane; i < G * D; i += 32) o[i] = 0;
+    }
+  }
 
-  // ---- block ids of this partition
-  int* s_blk = reinterpret_cast<int*>(smem + C::MAIN);
-  {
-    const int nblk = (len + bs_mask) >> bs_shift;
-    const int* bt = a.block_table + static_cast<size_t>(s) * a.max_blocks_per_seq + (t_begin >> bs_shift);
-    for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
-      int b = bt[i];
-      if (b < 0 || b >= a.num_blocks) {
-        raise_error(2u);  // KVQ_DEVERR_BLOCK_RANGE
-        b = 0;
+  // ---- total tiles T and the range's first sequence (block scan of tile counts)
+  long long T = 0;
+  if (S <= static_cast<int>(blockDim.x)) {  // one pass: a sequence per thread
+    const int s = threadIdx.x;
+    const long long v = s < S ? seq_tiles(a, s) : 0;
+    long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) scratch[4 + warp] = incl;
+    __syncthreads();
+    long long before = 0;
+    for (int w = 0; w < hpc; ++w) {
+      const long long x = scratch[4 + w];
+      T += x;
+      if (w < warp) before += x;
+    }
+    const long long r0 = range_start(a, T, k), excl = before + incl - v;
+    if (v > 0 && excl <= r0 && r0 < excl + v) {
+      scratch[1] = s;
+      scratch[2] = excl;
+    }
+    __syncthreads();
+  } else {  // many sequences: total first, then a chunked scan up to the range start
+    long long part = 0;
+    for (int s = threadIdx.x; s < S; s += blockDim.x) part += seq_tiles(a, s);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) scratch[4 + warp] = part;
+    __syncthreads();
+    for (int w = 0; w < hpc; ++w) T += scratch[4 + w];
+    __syncthreads();
+    const long long r0 = range_start(a, T, k);
+    long long running = 0;
+    for (int base = 0; base < S && running <= r0; base += blockDim.x) {
+      const int s = base + threadIdx.x;
+      const long long v = s < S ? seq_tiles(a, s) : 0;
+      long long incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      s_blk[i] = b;
+      if (lane == 31) scratch[4 + warp] = incl;
+      __syncthreads();
+      long long before = running;
+      for (int w = 0; w < warp; ++w) before += scratch[4 + w];
+      const long long excl = before + incl - v;
+      if (v > 0 && excl <= r0 && r0 < excl + v) {
+        scratch[1] = s;
+        scratch[2] = excl;
+      }
+      for (int w = 0; w < hpc; ++w) running += scratch[4 + w];
+      __syncthreads();
     }
+  }
+  const long long R0 = range_start(a, T, k), R1 = range_start(a, T, k + 1);
+  if (R0 >= R1) return;
+  const int n = static_cast<int>(R1 - R0);
+  const int s_first = static_cast<int>(scratch[1]);
+  const long long ps_first = scratch[2];
+  prefetch_q(s_first);
+
+  if (threadIdx.x == 0) {
+    scratch[0] = T;
+    scratch[3] = R1;
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(full_s + 8 * i, 1);
+      mbar_init(empty_s + 8 * i, hpc);
+    }
+    for (int i = 12; i < 16; ++i) scratch[i] = -1;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
 
-  // ---- per-warp pipeline over tiles warp, warp + W, ...; the first tiles are
-  // requested before the query is prepared so that the two overlap
-  uint8_t* ring = smem + warp * C::WARP_SMEM;
-  const uint32_t ring_s = smem_u32(ring);
-  const int my_tiles = ntiles > warp ? (ntiles - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
-  const uint32_t rowK = static_cast<uint32_t>(Hkv) * C::KB;  // bytes from one token row to the next
-  const uint32_t rowV = static_cast<uint32_t>(Hkv) * C::VB;
-  const uint32_t lane_k = 2 * g * rowK + h * C::KB + c * C::KPS;
-  const uint32_t lane_v = 4 * c * rowV + h * C::VB + g * C::VPS;
-
-  auto issue = [&](int it, int stage) {
-    const int tok0 = (warp + it * kDecodeWarps) * 16;
-    const int blk = s_blk[tok0 >> bs_shift];
-    const size_t trow = (static_cast<size_t>(blk) << bs_shift) + (tok0 & bs_mask);
-    const uint8_t* kb = a.k_cache + trow * rowK + lane_k;
-    const uint8_t* vb = a.v_cache + trow * rowV + lane_v;
-    const uint32_t st = ring_s + stage * C::STAGE;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-#pragma unroll
-      for (int pc = 0; pc < C::KP; ++pc)
-        cp_async<C::KPS>(st + ((r * C::KP + pc) * 32 + lane) * C::KPS, kb + r * rowK + pc * C::KSTRIDE_P);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      cp_async<C::VPS>(st + C::K_BYTES + (u * 32 + lane) * C::VPS, vb + u * rowV);
-    if constexpr (C::KMF + C::VMF > 0) {
-      if (lane < 2 * (C::KMF + C::VMF)) {
-        const int fidx = lane >> 1, half = lane & 1;
-        const bool isk = fidx < C::KMF;
-        const int f = isk ? fidx : fidx - C::KMF;
-        const int nf = isk ? C::KMF : C::VMF;
-        const __half* base = isk ? a.k_meta : a.v_meta;
-        const __half* src = base + ((static_cast<size_t>(blk) * Hkv + h) * nf + f) * a.block_size +
-                            (tok0 & bs_mask) + 8 * half;
-        cp_async<16>(st + C::K_BYTES + C::V_BYTES + fidx * 32 + half * 16, src);
+  // ---- producer cursor (thread 0): walks the range tile by tile
+  const uint32_t tile_bytes = hpc * (C::K_HEAD + C::V_HEAD) + hpc * (C::KMF + C::VMF) * 32;
+  const int bs_shift = a.block_shift, bs_mask = a.block_size - 1;
+  // The cursor lives in shared memory: only thread 0 uses it, and registers
+  // held by every thread for it would be taken from the consumers.
+  Cursor* cur = reinterpret_cast<Cursor*>(scratch + 16);
+  auto block_of = [&](const Cursor& u) {  // block id of the cursor's tile
+    return a.block_table[static_cast<size_t>(u.s) * a.max_blocks_per_seq + ((16 * u.t) >> bs_shift)];
+  };
+  auto find_next = [&](Cursor& u) {  // first sequence after u.s with tokens, if the range goes on
+    u.nx = S;
+    if (u.ps + u.tiles >= scratch[3]) return;
+    for (int s2 = u.s + 1; s2 < S; ++s2) {
+      const int cx = a.context_lens[s2];
+      const int cc = cx <= 0 ? 0 : min(cx, a.max_context_len);
+      if (cc > 0) {
+        u.nx = s2;
+        u.nx_ctx = cc;
+        return;
       }
     }
   };
-
-#pragma unroll
-  for (int i = 0; i < C::STAGES - 1; ++i) {
-    if (i < my_tiles) issue(i, i);
-    cp_async_commit();
+  if (threadIdx.x == 0) {
+    Cursor u;
+    u.ps = ps_first;
+    u.s = s_first;
+    u.t = static_cast<int>(R0 - ps_first);
+    u.ctx = min(a.context_lens[s_first], a.max_context_len);
+    u.tiles = (u.ctx + 15) >> 4;
+    u.blk = block_of(u);
+    u.nx_ctx = 0;
+    u.i = 0;
+    find_next(u);
+    *cur = u;
   }
-
-  // ---- query rows (fp32) of the G heads, rotated for KVarN
-  float* sq = reinterpret_cast<float*>(smem + C::RING);
-  for (int i = threadIdx.x; i < 8 * D; i += blockDim.x) {
-    const int n = i / D;
-    float v = 0.0f;
-    if (n < G) v = __uint_as_float(static_cast<uint32_t>(a.query[out_row0 * D + i]) << 16);
-    sq[i] = v;
-  }
-  __syncthreads();
-  if constexpr (KVARN) {
-    for (int n = warp; n < G; n += kDecodeWarps) rotate_row_warp<D, false>(sq + n * D, a.signs, a.cR, lane);
-    __syncthreads();
-  }
-  uint32_t qf[C::KSTEPS][2];
-  float qs = 0.0f;
-#pragma unroll
-  for (int j = 0; j < C::KSTEPS; ++j) {
-    float v[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      v[e] = __half2float(__float2half_rn(sq[g * D + kslot_d<D, KF>(c, j, e)]));
-      qs += v[e];
+  auto issue = [&](int st) {  // the cursor's tile into stage st, then advance the cursor
+    Cursor u = *cur;
+    TileHeader& hd = hdr[st];
+    hd.s = u.s;
+    hd.t = u.t;
+    hd.valid = min(16, u.ctx - 16 * u.t);
+    hd.flags = (u.i == 0 || u.t == 0 ? 1 : 0) | (u.i == n - 1 || u.t == u.tiles - 1 ? 2 : 0);
+    hd.ps = static_cast<int>(u.ps);
+    hd.tiles = u.tiles;
+    hd.next_s = u.nx < S ? u.nx : -1;
+    const int tok = 16 * u.t;
+    int blk = u.blk;
+    if (blk < 0 || blk >= a.num_blocks) {
+      raise_error(2u);  // KVQ_DEVERR_BLOCK_RANGE: read block 0 instead
+      blk = 0;
     }
-    qf[j][0] = pack_half2(v[0], v[1]);
-    qf[j][1] = pack_half2(v[2], v[3]);
-  }
-  qs += __shfl_xor_sync(0xffffffffu, qs, 1);
-  qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-  const float qsum0 = __shfl_sync(0xffffffffu, qs, (2 * c) * 4);
-  const float qsum1 = __shfl_sync(0xffffffffu, qs, (2 * c + 1) * 4);
+    const int off = tok & bs_mask;
+    const uint32_t sb = base_s + st * stage_bytes;
+    const uint32_t bar = full_s + 8 * st;
+    mbar_arrive_expect(bar, tile_bytes);
+    if (a.one_box) {
+      tma_load_4d(sb, &maps.k, 0, off, hg * hpc, blk, bar);
+      tma_load_4d(sb + v_off, &maps.v, 0, off, hg * hpc, blk, bar);
+    } else {
+      for (int hh = 0; hh < hpc; ++hh) {
+        tma_load_4d(sb + hh * C::K_HEAD, &maps.k, 0, hg * hpc + hh, off, blk, bar);
+        tma_load_4d(sb + v_off + hh * C::V_HEAD, &maps.v, 0, hg * hpc + hh, off, blk, bar);
+      }
+    }
+    if constexpr (C::KMF > 0) tma_load_4d(sb + m_off, &maps.km, off, 0, hg * hpc, blk, bar);
+    if constexpr (C::VMF > 0) tma_load_4d(sb + vm_off, &maps.vm, off, 0, hg * hpc, blk, bar);
+    ++u.i;
+    if (++u.t == u.tiles && u.i < n) {  // on to the next sequence with tokens
+      u.ps += u.tiles;
+      u.t = 0;
+      if (u.nx >= S) {  // cannot happen with the tile count T; stay in bounds
+        raise_error(4u);
+        u.nx = S - 1;
+        u.nx_ctx = 16;
+      }
+      u.s = u.nx;
+      u.ctx = u.nx_ctx;
+      u.tiles = (u.ctx + 15) >> 4;
+      find_next(u);
+    }
+    if (u.i < n) u.blk = block_of(u);  // prefetched: consumed by the next issue
+    *cur = u;
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < C::STAGES && i < n; ++i) issue(i);
 
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
-  float O[C::DTILES][4];
+  // ---- per-lane shared-memory addresses inside a stage (swizzled boxes)
+  const int row0 = tile_row(g), row1 = tile_row(g + 8);
+  uint32_t k_addr[2][C::KP];
 #pragma unroll
-  for (int i = 0; i < C::DTILES; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+  for (int pc = 0; pc < C::KP; ++pc) {
+    const int chunk = (pc * C::KSTRIDE_P + c * C::KPS) / 16, byte = (c * C::KPS) % 16;
+    k_addr[0][pc] = swz_addr<C::KB, C::K_SWZ>(warp * C::K_HEAD, row0, chunk, byte);
+    k_addr[1][pc] = swz_addr<C::KB, C::K_SWZ>(warp * C::K_HEAD, row1, chunk, byte);
+  }
+  uint32_t v_addr[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    v_addr[u] = v_off + swz_addr<C::VB, C::V_SWZ>(warp * C::V_HEAD, v_token(c, u),
+                                                  (g * C::VPS) / 16, (g * C::VPS) % 16);
+  const uint32_t meta_k = m_off + warp * C::KMF * 32;
+  const uint32_t meta_v = vm_off + warp * C::VMF * 32;
+  const float vsc = is_asym(VF) ? 1.0f : a.v_scale;
 
-  int stage = 0;
-  for (int it = 0; it < my_tiles; ++it) {
-    cp_async_wait<C::STAGES - 2>();
-    __syncwarp();
-    const uint8_t* st = ring + stage * C::STAGE;
-    const int valid = len - (warp + it * kDecodeWarps) * 16;
+  uint32_t qf[C::KSTEPS][2];
+  float qsum0 = 0.f, qsum1 = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+  // PV accumulators as the output runs they become: lane (g, c) holds dims
+  // g*E .. g*E+E-1 of query heads 2c (Oa) and 2c+1 (Ob)
+  constexpr int E = 2 * C::DTILES;
+  float Oa[E], Ob[E];
+  int seg_t0 = 0;
+  bool healthy = true;
+  bool first_seg = true;  // the range's first segment (slot 0 if partial; slot 1 otherwise)
 
+  int st = 0;
+  uint32_t phase = 0;
+  for (int i = 0; i < n; ++i) {
+    if (!mbar_wait(full_s + 8 * st, phase)) healthy = false;
+    const TileHeader hd = hdr[st];
+    const uint32_t sb = base_s + st * stage_bytes;
+    const size_t out_row0 = static_cast<size_t>(hd.s) * a.num_q_heads + static_cast<size_t>(h) * G;
+
+    if (hd.flags & 1) {  // a new segment: this warp's query fragment, fresh state
+      cp_async_wait<0>();  // the rows were fetched during the previous segment
+      __syncwarp();
+      float qs = 0.0f;
+      if constexpr (KVARN) {
+        float* srow = reinterpret_cast<float*>(smem + rot_off + warp * D * 4);
+        float qv[C::KSTEPS][4];
+        for (int nn = 0; nn < G; ++nn) {
+          for (int e = lane; e < D; e += 32)
+            srow[e] = __uint_as_float(static_cast<uint32_t>(lds_u16(qbuf_s + 2 * (nn * D + e))) << 16);
+          __syncwarp();
+          rotate_row_warp<D, false>(srow, a.signs, a.cR, lane);
+          if (g == nn) {
+#pragma unroll
+            for (int j = 0; j < C::KSTEPS; ++j)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) qv[j][e] = srow[kslot_d<D, KF>(c, j, e)];
+          }
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < C::KSTEPS; ++j) {
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[e] = g < G ? __half2float(__float2half_rn(qv[j][e])) : 0.0f;
+            qs += v[e];
+          }
+          qf[j][0] = pack_half2(v[0], v[1]);
+          qf[j][1] = pack_half2(v[2], v[3]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < C::KSTEPS; ++j) {
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[e] = 0.0f;
+            if (g < G)
+              v[e] = __half2float(__float2half_rn(__uint_as_float(
+                  static_cast<uint32_t>(lds_u16(qbuf_s + 2 * (g * D + kslot_d<D, KF>(c, j, e)))) << 16)));
+            qs += v[e];
+          }
+          qf[j][0] = pack_half2(v[0], v[1]);
+          qf[j][1] = pack_half2(v[2], v[3]);
+        }
+      }
+      __syncwarp();  // every lane has read the rows: fetch the next segment's
+      if (hd.next_s >= 0) prefetch_q(hd.next_s);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+      qsum0 = __shfl_sync(0xffffffffu, qs, (2 * c) * 4);
+      qsum1 = __shfl_sync(0xffffffffu, qs, (2 * c + 1) * 4);
+      m0 = m1 = -INFINITY;
+      l0 = l1 = z0 = z1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) Oa[e] = Ob[e] = 0.f;
+      seg_t0 = hd.t;
+    }
+    const int valid = hd.valid;
+
+    // ---- K rows (and K metadata) of the stage into registers
     uint32_t kw[2][C::KW];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
 #pragma unroll
       for (int pc = 0; pc < C::KP; ++pc) {
-        const uint8_t* src = st + ((r * C::KP + pc) * 32 + lane) * C::KPS;
         if constexpr (C::KPS == 16) {
-          const uint4 w = *reinterpret_cast<const uint4*>(src);
+          const uint4 w = lds128(sb + k_addr[r][pc]);
           kw[r][pc * 4 + 0] = w.x; kw[r][pc * 4 + 1] = w.y;
           kw[r][pc * 4 + 2] = w.z; kw[r][pc * 4 + 3] = w.w;
         } else {
-          const uint2 w = *reinterpret_cast<const uint2*>(src);
+          const uint2 w = lds64(sb + k_addr[r][pc]);
           kw[r][pc * 2 + 0] = w.x; kw[r][pc * 2 + 1] = w.y;
         }
       }
-      if constexpr (KF == INT8) {
-#pragma unroll
-        for (int k = 0; k < C::KW; ++k) kw[r][k] ^= 0x80808080u;
+    }
+    float ks0 = 1.f, ks1 = 1.f, kz0 = 0.f, kz1 = 0.f, vs0 = 1.f, vs1 = 1.f, vz0 = 0.f, vz1 = 0.f;
+    if constexpr (is_asym(KF)) {
+      const uint32_t mk = sb + meta_k;
+      ks0 = lds_half(mk + 2 * row0); ks1 = lds_half(mk + 2 * row1);
+      kz0 = lds_half(mk + 32 + 2 * row0); kz1 = lds_half(mk + 32 + 2 * row1);
+      if constexpr (KVARN) {
+        const float sg0 = lds_half(mk + 64 + 2 * row0), sg1 = lds_half(mk + 64 + 2 * row1);
+        ks0 *= sg0; kz0 *= sg0; ks1 *= sg1; kz1 *= sg1;
       }
     }
-
+    if constexpr (KF == INT8) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int q = 0; q < C::KW; ++q) kw[r][q] ^= 0x80808080u;
+    }
     // ---- S^T = K q^T (two accumulators halve the dependent mma chain)
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sbb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < C::KSTEPS; ++j) {
       uint32_t a0, a1, a2, a3;
       k_frag<KF, C::KW>(kw, j, a0, a1, a2, a3);
-      if (j & 1) mma16816(sb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+      if (j & 1) mma16816(sbb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
       else mma16816(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
     }
-    float sacc[4];
+    float sl[4];
+    {
+      float sacc[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sacc[k] = sa[k] + sb[k];
+      for (int q = 0; q < 4; ++q) sacc[q] = sa[q] + sbb[q];
+      if constexpr (!is_asym(KF)) {
+        constexpr float bias = KF == INT8 ? 1152.0f : 0.0f;
+        sl[0] = (sacc[0] - bias * qsum0) * a.qk_scale;
+        sl[1] = (sacc[1] - bias * qsum1) * a.qk_scale;
+        sl[2] = (sacc[2] - bias * qsum0) * a.qk_scale;
+        sl[3] = (sacc[3] - bias * qsum1) * a.qk_scale;
+      } else {
+        sl[0] = (ks0 * (sacc[0] - 1024.0f * qsum0) + kz0 * qsum0) * a.qk_scale;
+        sl[1] = (ks0 * (sacc[1] - 1024.0f * qsum1) + kz0 * qsum1) * a.qk_scale;
+        sl[2] = (ks1 * (sacc[2] - 1024.0f * qsum0) + kz1 * qsum0) * a.qk_scale;
+        sl[3] = (ks1 * (sacc[3] - 1024.0f * qsum1) + kz1 * qsum1) * a.qk_scale;
+      }
+    }
+    const bool ok0 = row0 < valid, ok1 = row1 < valid;
+    if (!ok0) sl[0] = sl[1] = -INFINITY;
+    if (!ok1) sl[2] = sl[3] = -INFINITY;
 
+    // ---- V rows (and V metadata), then release the stage
     uint32_t vw[4][C::VW];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const uint8_t* src = st + C::K_BYTES + (u * 32 + lane) * C::VPS;
       if constexpr (C::VPS == 16) {
-        const uint4 w = *reinterpret_cast<const uint4*>(src);
+        const uint4 w = lds128(sb + v_addr[u]);
         vw[u][0] = w.x; vw[u][1] = w.y; vw[u][2] = w.z; vw[u][3] = w.w;
       } else if constexpr (C::VPS == 8) {
-        const uint2 w = *reinterpret_cast<const uint2*>(src);
+        const uint2 w = lds64(sb + v_addr[u]);
         vw[u][0] = w.x; vw[u][1] = w.y;
       } else {
-        vw[u][0] = *reinterpret_cast<const uint32_t*>(src);
+        vw[u][0] = lds32(sb + v_addr[u]);
       }
-      if constexpr (VF == INT8) {
+    }
+    if constexpr (is_asym(VF)) {
+      const uint32_t mv = sb + meta_v;
+      vs0 = lds_half(mv + 2 * row0); vs1 = lds_half(mv + 2 * row1);
+      vz0 = lds_half(mv + 32 + 2 * row0); vz1 = lds_half(mv + 32 + 2 * row1);
+      if constexpr (KVARN) {
+        const float sg0 = lds_half(mv + 64 + 2 * row0), sg1 = lds_half(mv + 64 + 2 * row1);
+        vs0 *= sg0; vz0 *= sg0; vs1 *= sg1; vz1 *= sg1;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_s + 8 * st);
+    if (threadIdx.x == 0 && cur->i < n) {  // refill this stage once every warp has read it
+      if (mbar_wait(empty_s + 8 * st, phase)) issue(st);
+      else raise_error(16u);  // KVQ_DEVERR_TIMEOUT
+    }
+    __syncwarp();
+
+    if constexpr (VF == INT8) {
 #pragma unroll
-        for (int k = 0; k < C::VW; ++k) vw[u][k] ^= 0x80808080u;
-      }
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < C::VW; ++q) vw[u][q] ^= 0x80808080u;
     }
     if (valid < 16) {
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (4 * c + u >= valid) {
+        if (v_token(c, u) >= valid) {
 #pragma unroll
-          for (int k = 0; k < C::VW; ++k) vw[u][k] = (VF == INT8) ? 0x80808080u : 0u;
+          for (int q = 0; q < C::VW; ++q) vw[u][q] = (VF == INT8) ? 0x80808080u : 0u;
         }
     }
-    const uint8_t* meta = st + C::K_BYTES + C::V_BYTES;
-    float sl[4];
-    if constexpr (!is_asym(KF)) {
-      constexpr float bias = KF == INT8 ? 1152.0f : 0.0f;
-      sl[0] = (sacc[0] - bias * qsum0) * a.qk_scale;
-      sl[1] = (sacc[1] - bias * qsum1) * a.qk_scale;
-      sl[2] = (sacc[2] - bias * qsum0) * a.qk_scale;
-      sl[3] = (sacc[3] - bias * qsum1) * a.qk_scale;
-    } else {
-      const float2 ks = __half22float2(*reinterpret_cast<const __half2*>(meta + 0 * 32 + 4 * g));
-      const float2 kz = __half22float2(*reinterpret_cast<const __half2*>(meta + 1 * 32 + 4 * g));
-      float ks0 = ks.x, ks1 = ks.y, kz0 = kz.x, kz1 = kz.y;
-      if constexpr (KVARN) {
-        const float2 ksg = __half22float2(*reinterpret_cast<const __half2*>(meta + 2 * 32 + 4 * g));
-        ks0 *= ksg.x; kz0 *= ksg.x; ks1 *= ksg.y; kz1 *= ksg.y;
-      }
-      sl[0] = (ks0 * (sacc[0] - 1024.0f * qsum0) + kz0 * qsum0) * a.qk_scale;
-      sl[1] = (ks0 * (sacc[1] - 1024.0f * qsum1) + kz0 * qsum1) * a.qk_scale;
-      sl[2] = (ks1 * (sacc[2] - 1024.0f * qsum0) + kz1 * qsum0) * a.qk_scale;
-      sl[3] = (ks1 * (sacc[3] - 1024.0f * qsum1) + kz1 * qsum1) * a.qk_scale;
-    }
-    const bool ok0 = 2 * g < valid, ok1 = 2 * g + 1 < valid;
-    if (!ok0) sl[0] = sl[1] = -INFINITY;
-    if (!ok1) sl[2] = sl[3] = -INFINITY;
+
 
     // ---- online softmax (log2 domain), lazy rescale: the running maximum m is
     // only raised (with a reduction over the tile) when some logit exceeds it
@@ -413,9 +966,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeMinBlocks)
       m1 = n1;
       l0 *= al0; l1 *= al1; z0 *= al0; z1 *= al1;
 #pragma unroll
-      for (int i = 0; i < C::DTILES; ++i) {
-        O[i][0] *= al0; O[i][2] *= al0;
-        O[i][1] *= al1; O[i][3] *= al1;
+      for (int d = 0; d < C::DTILES; ++d) {
+        Oa[2 * d] *= al0; Oa[2 * d + 1] *= al0;
+        Ob[2 * d] *= al1; Ob[2 * d + 1] *= al1;
       }
     }
     float pr[4];
@@ -426,13 +979,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeMinBlocks)
     l0 += pr[0] + pr[2];
     l1 += pr[1] + pr[3];
     if constexpr (is_asym(VF)) {
-      const float2 vs = __half22float2(*reinterpret_cast<const __half2*>(meta + (C::KMF + 0) * 32 + 4 * g));
-      const float2 vz = __half22float2(*reinterpret_cast<const __half2*>(meta + (C::KMF + 1) * 32 + 4 * g));
-      float vs0 = vs.x, vs1 = vs.y, vz0 = vz.x, vz1 = vz.y;
-      if constexpr (KVARN) {
-        const float2 vsg = __half22float2(*reinterpret_cast<const __half2*>(meta + (C::KMF + 2) * 32 + 4 * g));
-        vs0 *= vsg.x; vz0 *= vsg.x; vs1 *= vsg.y; vz1 *= vsg.y;
-      }
       if (!ok0) vs0 = vz0 = 0.f;
       if (!ok1) vs1 = vz1 = 0.f;
       z0 += pr[0] * vz0 + pr[2] * vz1;
@@ -440,10 +986,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeMinBlocks)
       pr[0] *= vs0; pr[1] *= vs0;
       pr[2] *= vs1; pr[3] *= vs1;
     }
-    // ---- P^T operand: lane (g, c) needs head g, tokens 4c..4c+3
-    const uint32_t x0 = pack_half2(pr[0], pr[2]);  // head 2c, tokens (2g, 2g+1)
+    // ---- P^T operand: lane (g, c) needs head g at its 4 V tokens
+    const uint32_t x0 = pack_half2(pr[0], pr[2]);  // head 2c, rows (g, g+8)
     const uint32_t x1 = pack_half2(pr[1], pr[3]);  // head 2c+1
-    const int src0 = (2 * c) * 4 + (g >> 1), src1 = (2 * c + 1) * 4 + (g >> 1);
+    const int src0 = c * 4 + (g >> 1), src1 = (c + 4) * 4 + (g >> 1);
     const uint32_t u0 = __shfl_sync(0xffffffffu, x0, src0);
     const uint32_t u1 = __shfl_sync(0xffffffffu, x1, src0);
     const uint32_t u2 = __shfl_sync(0xffffffffu, x0, src1);
@@ -452,151 +998,115 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, kDecodeMinBlocks)
     const uint32_t b1 = (g & 1) ? u3 : u2;
     // ---- O^T += V^T P^T
 #pragma unroll
-    for (int i = 0; i < C::DTILES; ++i) {
+    for (int d = 0; d < C::DTILES; ++d) {
       uint32_t a0, a1, a2, a3;
-      v_frag<VF, C::VW>(vw, i, a0, a1, a2, a3);
-      mma16816(O[i], a0, a1, a2, a3, b0, b1);
+      v_frag<VF, C::VW>(vw, d, a0, a1, a2, a3);
+      mma16816(Oa[2 * d], Ob[2 * d], Oa[2 * d + 1], Ob[2 * d + 1], a0, a1, a2, a3, b0, b1);
     }
-    __syncwarp();
-    const int nx = it + C::STAGES - 1;
-    if (nx < my_tiles) issue(nx, stage == 0 ? C::STAGES - 1 : stage - 1);
-    cp_async_commit();
-    stage = stage + 1 == C::STAGES ? 0 : stage + 1;
-  }
-  cp_async_wait<0>();
+    if (++st == C::STAGES) {
+      st = 0;
+      phase ^= 1u;
+    }
+    if (!(hd.flags & 2)) continue;
 
+    // ================= end of this CTA's segment of sequence hd.s =================
+    if (!healthy && lane == 0) raise_error(16u);  // KVQ_DEVERR_TIMEOUT (garbage results)
+    float L0 = l0, L1 = l1, Z0 = z0, Z1 = z1;
 #pragma unroll
-  for (int o = 4; o <= 16; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    z0 += __shfl_xor_sync(0xffffffffu, z0, o);
-    z1 += __shfl_xor_sync(0xffffffffu, z1, o);
-  }
-  __syncthreads();  // every ring is drained; reuse shared memory for the combine
-
-  float* cO = reinterpret_cast<float*>(smem);        // [W][8][D]
-  float* cM = cO + kDecodeWarps * 8 * D;             // [W][8]
-  float* cL = cM + kDecodeWarps * 8;                 // [W][8]
-  float* cRes = cL + kDecodeWarps * 8;               // [8][D] (direct KVarN output)
-#pragma unroll
-  for (int i = 0; i < C::DTILES; ++i) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int d = g * (D / 8) + 2 * i + r;
-      cO[(warp * 8 + 2 * c) * D + d] = O[i][2 * r] + z0;
-      cO[(warp * 8 + 2 * c + 1) * D + d] = O[i][2 * r + 1] + z1;
+    for (int o = 4; o <= 16; o <<= 1) {
+      L0 += __shfl_xor_sync(0xffffffffu, L0, o);
+      L1 += __shfl_xor_sync(0xffffffffu, L1, o);
+      Z0 += __shfl_xor_sync(0xffffffffu, Z0, o);
+      Z1 += __shfl_xor_sync(0xffffffffu, Z1, o);
     }
-  }
-  if (g == 0) {
-    cM[warp * 8 + 2 * c] = m0;
-    cM[warp * 8 + 2 * c + 1] = m1;
-    cL[warp * 8 + 2 * c] = l0;
-    cL[warp * 8 + 2 * c + 1] = l1;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int n = i / D, d = i % D;
-    float M = -INFINITY;
+    const bool whole = seg_t0 == 0 && hd.t == hd.tiles - 1;
+    const int j = first_seg ? 0 : 1;
+    first_seg = false;
+    {
+      const float sc0 = whole ? vsc / L0 : vsc, sc1 = whole ? vsc / L1 : vsc;
 #pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, cM[w * 8 + n]);
-    float acc = 0.f, L = 0.f;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) {
-      const float mw = cM[w * 8 + n];
-      if (mw == -INFINITY) continue;
-      const float wt = fast_exp2(mw - M);
-      acc += wt * cO[(w * 8 + n) * D + d];
-      L += wt * cL[w * 8 + n];
-    }
-    if constexpr (!is_asym(VF)) acc *= a.v_scale;
-    if (direct) {
-      const float res = acc / L;
-      if constexpr (KVARN) cRes[i] = res;
-      else a.out[out_row0 * D + i] = f2bf(res);
-    } else {
-      const size_t r = (out_row0 + n) * a.num_partitions + p;
-      a.ws_acc[r * D + d] = acc;
-      if (d == 0) {
-        a.ws_ml[2 * r] = M;
-        a.ws_ml[2 * r + 1] = L;
+      for (int e = 0; e < E; ++e) {
+        Oa[e] = (Oa[e] + Z0) * sc0;
+        Ob[e] = (Ob[e] + Z1) * sc1;
       }
     }
-  }
-  if (direct) {
-    if constexpr (KVARN) {
-      __syncthreads();
-      for (int n = warp; n < G; n += kDecodeWarps) rotate_row_warp<D, true>(cRes + n * D, a.signs, a.cR, lane);
-      __syncthreads();
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x) a.out[out_row0 * D + i] = f2bf(cRes[i]);
+    if (whole) {  // the whole sequence lies in this range: write the output
+      if constexpr (KVARN) {  // inverse rotation: x = d . (cR * H y)
+        fwht_accum_rows<E>(Oa, g);
+        fwht_accum_rows<E>(Ob, g);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int dd = g * E + e;
+          const float sgn = (a.signs != nullptr && a.signs[dd] < 0) ? -1.f : 1.f;
+          Oa[e] = __fmul_rn(Oa[e], a.cR) * sgn;
+          Ob[e] = __fmul_rn(Ob[e], a.cR) * sgn;
+        }
+      }
+      if (2 * c < G) store_bf16_run<E>(a.out + (out_row0 + 2 * c) * D + g * E, Oa);
+      if (2 * c + 1 < G) store_bf16_run<E>(a.out + (out_row0 + 2 * c + 1) * D + g * E, Ob);
+      continue;
     }
-    return;
+
+    // ---- part of a sequence: (m, l, acc) into this range's slot, then publish
+    const size_t slot = ((static_cast<size_t>(k) * HG + hg) * 2 + j) * (hpc * G) + warp * G;
+    if (2 * c < G) store_f32_run<E>(a.ws_acc + (slot + 2 * c) * D + g * E, Oa);
+    if (2 * c + 1 < G) store_f32_run<E>(a.ws_acc + (slot + 2 * c + 1) * D + g * E, Ob);
+    if (g == 0) {
+      if (2 * c < G) *reinterpret_cast<float2*>(a.ws_ml + 2 * (slot + 2 * c)) = make_float2(m0, L0);
+      if (2 * c + 1 < G)
+        *reinterpret_cast<float2*>(a.ws_ml + 2 * (slot + 2 * c + 1)) = make_float2(m1, L1);
+    }
+    if (warp != pub) {
+      bar_arrive(1 + j, hpc * 32);  // hand the stores to the publishing warp; go on
+    } else {
+      bar_sync(1 + j, hpc * 32);
+      if (lane == 0) {
+        __threadfence();  // every warp's slot stores before the tag
+        st_relaxed_u64(a.tags + (static_cast<size_t>(k) * HG + hg) * 2 + j, a.epoch);
+        scratch[12 + 2 * j] = hd.ps;
+        scratch[13 + 2 * j] = (static_cast<long long>(hd.s) << 32) | hd.tiles;
+      }
+      __syncwarp();
+    }
   }
 
-  // ---- the last CTA to finish a (sequence, kv-head) merges its partitions
-  __threadfence();
+  // ---- merges: a partial segment is merged here once every other range of its
+  // sequence has published (a fence between this CTA's tag stores and its loads)
   __syncthreads();
-  int* s_last = reinterpret_cast<int*>(smem + C::MAIN);  // block ids are dead by now
-  const int np_s = (ctx + P - 1) / P;
-  if (threadIdx.x == 0) {
-    unsigned long long* ctr = a.counters + static_cast<size_t>(s) * Hkv + h;
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), assumed, nv = 0;
-    int tries = 0;
-    do {  // counters carry the call's epoch: stale contents from any earlier use are reset
-      assumed = old;
-      nv = ((assumed >> 16) == a.epoch) ? assumed + 1 : ((a.epoch << 16) | 1ull);
-      old = atomicCAS(ctr, assumed, nv);
-    } while (old != assumed && ++tries < (1 << 20));
-    if (old != assumed) raise_error(8u);  // KVQ_DEVERR_COMBINE
-    s_last[0] = (old == assumed) && static_cast<int>(nv & 0xFFFFull) == np_s;
+  const long long Tm = scratch[0];
+  if (warp == pub) {
+    __threadfence();
+#pragma unroll 1
+    for (int jj = 0; jj < 2; ++jj) {
+      const long long info = scratch[13 + 2 * jj];
+      if (info < 0) continue;
+      const long long ps = scratch[12 + 2 * jj];
+      const int tiles = static_cast<int>(info & 0xFFFFFFFFll);
+      const int ka = range_of(a, ps, Tm), kb = range_of(a, ps + tiles - 1, Tm);
+      bool done = true;
+      for (int kk = ka + lane; kk <= kb; kk += 32) {
+        const long long q0 = range_start(a, Tm, kk), q1 = range_start(a, Tm, kk + 1);
+        if (kk == k || q0 >= q1) continue;  // this range, or an empty one
+        const int j2 = (q0 >= ps) ? 0 : 1;
+        if (ld_relaxed_u64(a.tags + (static_cast<size_t>(kk) * HG + hg) * 2 + j2) != a.epoch)
+          done = false;
+      }
+      done = __all_sync(0xffffffffu, done);
+      if (lane == 0) {  // one merge per sequence: the first to swap the tag into its claim word
+        if (!done || atomicExch(a.claims + static_cast<size_t>(info >> 32) * HG + hg, a.epoch) == a.epoch)
+          scratch[13 + 2 * jj] = -1;
+      }
+      __syncwarp();
+    }
+    __threadfence();
   }
   __syncthreads();
-  if (!s_last[0]) return;
-  __threadfence();
-  float* sW = reinterpret_cast<float*>(smem);  // [8][np_s] partition weights
-  float* sLinv = sW + 8 * kMaxPartitions;      // [8]
-  float* sRes = sLinv + 8;                     // [8][D]
-  for (int n = warp; n < G; n += kDecodeWarps) {
-    const size_t r0 = (out_row0 + n) * a.num_partitions;
-    float M = -INFINITY;
-    for (int q = lane; q < np_s; q += 32) M = fmaxf(M, __ldcg(a.ws_ml + 2 * (r0 + q)));
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-    for (int q = lane; q < np_s; q += 32) {
-      const float w = fast_exp2(__ldcg(a.ws_ml + 2 * (r0 + q)) - M);
-      sW[n * np_s + q] = w;
-      L += w * __ldcg(a.ws_ml + 2 * (r0 + q) + 1);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) sLinv[n] = 1.0f / L;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < G * (D / 4); i += blockDim.x) {
-    const int n = i / (D / 4), d4 = (i % (D / 4)) * 4;
-    const float4* src = reinterpret_cast<const float4*>(a.ws_acc + (out_row0 + n) * a.num_partitions * D + d4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int q = 0; q < np_s; ++q) {
-      const float4 v = __ldcg(src + static_cast<size_t>(q) * (D / 4));
-      const float w = sW[n * np_s + q];
-      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-    }
-    const float li = sLinv[n];
-    if constexpr (KVARN) {
-      sRes[n * D + d4 + 0] = acc.x * li; sRes[n * D + d4 + 1] = acc.y * li;
-      sRes[n * D + d4 + 2] = acc.z * li; sRes[n * D + d4 + 3] = acc.w * li;
-    } else {
-      uint16_t* o = a.out + (out_row0 + n) * D + d4;
-      o[0] = f2bf(acc.x * li); o[1] = f2bf(acc.y * li);
-      o[2] = f2bf(acc.z * li); o[3] = f2bf(acc.w * li);
-    }
-  }
-  if constexpr (KVARN) {
-    __syncthreads();
-    for (int n = warp; n < G; n += kDecodeWarps) rotate_row_warp<D, true>(sRes + n * D, a.signs, a.cR, lane);
-    __syncthreads();
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) a.out[out_row0 * D + i] = f2bf(sRes[i]);
+#pragma unroll 1
+  for (int pm = 0; pm < 2; ++pm) {
+    const long long info = scratch[13 + 2 * pm];
+    if (info < 0) continue;
+    merge_partials<D, KVARN>(a, static_cast<int>(info >> 32), scratch[12 + 2 * pm],
+                             static_cast<int>(info & 0xFFFFFFFFll), Tm, NC, HG, hg, warp, lane, hpc);
   }
 }
 

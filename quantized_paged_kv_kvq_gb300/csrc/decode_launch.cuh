@@ -1,6 +1,9 @@
-// Launch of the decode kernel for one template instance (one launch: the last
-// CTA of each (sequence, kv-head) merges its partitions).
+// Launch of the decode kernel for one template instance: TMA descriptors of the
+// caller's cache arrays, then one launch (the last CTA of each sequence and
+// head group merges its partitions).
 #pragma once
+
+#include <cudaTypedefs.h>
 
 #include <atomic>
 
@@ -8,22 +11,111 @@
 
 namespace kvq {
 
+// cuTensorMapEncodeTiled, fetched once through the runtime (no libcuda link).
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+inline CUtensorMapSwizzle swizzle_mode(int bits) {
+  return bits == 3 ? CU_TENSOR_MAP_SWIZZLE_128B
+                   : bits == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
+}
+
+// Codes [NB, bs, Hkv, row] bytes: dims (row, Hkv, bs, NB), box = one head's
+// 16 tokens.
+inline bool encode_codes_map(CUtensorMap* m, const void* base, int row, int hkv, int bs, int nb,
+                             int swz_bits) {
+  const cuuint64_t dims[4] = {cuuint64_t(row), cuuint64_t(hkv), cuuint64_t(bs), cuuint64_t(nb)};
+  const cuuint64_t strides[3] = {cuuint64_t(row), cuuint64_t(row) * hkv,
+                                 cuuint64_t(row) * hkv * bs};
+  const cuuint32_t box[4] = {cuuint32_t(row), 1, 16, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle_mode(swz_bits), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Codes again, dims ordered (row, bs, Hkv, NB): one box of 16 tokens x hpc heads
+// lands head-major ([head][token][row]) in shared memory, the layout of hpc
+// single-head boxes, with one TMA instead of hpc.  Every address it can reach is
+// inside the cache; if the encoder rejects the ordering, per-head boxes are used.
+inline bool encode_codes_map_headmajor(CUtensorMap* m, const void* base, int row, int hkv, int bs,
+                                       int nb, int hpc, int swz_bits) {
+  const cuuint64_t dims[4] = {cuuint64_t(row), cuuint64_t(bs), cuuint64_t(hkv), cuuint64_t(nb)};
+  const cuuint64_t strides[3] = {cuuint64_t(row) * hkv, cuuint64_t(row),
+                                 cuuint64_t(row) * hkv * bs};
+  const cuuint32_t box[4] = {cuuint32_t(row), 16, cuuint32_t(hpc), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              swizzle_mode(swz_bits), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Metadata [NB, Hkv, F, bs] fp16: dims (bs, F, Hkv, NB), box = 16 tokens x F x hpc.
+inline bool encode_meta_map(CUtensorMap* m, const void* base, int nf, int hkv, int bs, int nb,
+                            int hpc) {
+  const cuuint64_t dims[4] = {cuuint64_t(bs), cuuint64_t(nf), cuuint64_t(hkv), cuuint64_t(nb)};
+  const cuuint64_t strides[3] = {cuuint64_t(bs) * 2, cuuint64_t(bs) * 2 * nf,
+                                 cuuint64_t(bs) * 2 * nf * hkv};
+  const cuuint32_t box[4] = {16, cuuint32_t(nf), cuuint32_t(hpc), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int KF, int VF, bool KVARN>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   using C = DecodeCfg<D, KF, VF, KVARN>;
+  if (tensor_map_encoder() == nullptr) return cudaErrorNotSupported;
+  DecodeMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  const int hpc = a.heads_per_cta;
+  DecodeArgs args = a;
+  args.one_box = encode_codes_map_headmajor(&maps.k, a.k_cache, C::KB, a.num_kv_heads,
+                                            a.block_size, a.num_blocks, hpc, C::K_SWZ) &&
+                 encode_codes_map_headmajor(&maps.v, a.v_cache, C::VB, a.num_kv_heads,
+                                            a.block_size, a.num_blocks, hpc, C::V_SWZ);
+  if (!args.one_box &&
+      (!encode_codes_map(&maps.k, a.k_cache, C::KB, a.num_kv_heads, a.block_size, a.num_blocks,
+                         C::K_SWZ) ||
+       !encode_codes_map(&maps.v, a.v_cache, C::VB, a.num_kv_heads, a.block_size, a.num_blocks,
+                         C::V_SWZ)))
+    return cudaErrorInvalidValue;
+  if (C::KMF > 0 && !encode_meta_map(&maps.km, a.k_meta, C::KMF, a.num_kv_heads, a.block_size,
+                                     a.num_blocks, hpc))
+    return cudaErrorInvalidValue;
+  if (C::VMF > 0 && !encode_meta_map(&maps.vm, a.v_meta, C::VMF, a.num_kv_heads, a.block_size,
+                                     a.num_blocks, hpc))
+    return cudaErrorInvalidValue;
+
   auto kern = decode_partition_kernel<D, KF, VF, KVARN>;
+  const int smem = decode_smem_bytes<C>(hpc, a.gqa);
   static std::atomic<unsigned long long> attr_done{0};  // one bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_done.load() & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             decode_smem_bytes<C>(kHeadsPerCta, 8));
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
-  const dim3 grid(a.num_kv_heads, a.num_seqs, a.num_partitions);
-  kern<<<grid, kDecodeWarps * 32, C::SMEM, st>>>(a);
+  const dim3 grid(a.num_ctas, a.num_kv_heads / hpc, 1);
+  kern<<<grid, hpc * 32, smem, st>>>(args, maps);
   return cudaGetLastError();
 }
 

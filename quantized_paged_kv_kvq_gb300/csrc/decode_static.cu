@@ -50,10 +50,10 @@ kvq_status kvq_paged_decode_static(const kvq_cache_desc* cache, const void* k_ca
                                    int32_t num_seqs, int32_t num_q_heads,
                                    const int32_t* block_table, int32_t max_blocks_per_seq,
                                    const int32_t* context_lens, int32_t max_context_len,
-                                   float sm_scale, int32_t partition_tokens, kvq_stream_t stream) {
+                                   float sm_scale, int32_t num_ctas, kvq_stream_t stream) {
   size_t need = 0;
   kvq_status st = kvq_decode_workspace_size_ex(cache, num_seqs, num_q_heads, max_context_len,
-                                               partition_tokens, &need);
+                                               num_ctas, &need);
   if (st != KVQ_OK) return st;
   if (need > kStaticScratchBytes) return KVQ_ERR_WORKSPACE;  // sizes beyond the fixed scratch
   void* scratch = nullptr;
@@ -63,7 +63,7 @@ kvq_status kvq_paged_decode_static(const kvq_cache_desc* cache, const void* k_ca
   }
   return kvq_paged_decode_ex(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads,
                              block_table, max_blocks_per_seq, context_lens, max_context_len,
-                             sm_scale, partition_tokens, scratch, need ? kStaticScratchBytes : 0,
+                             sm_scale, num_ctas, scratch, need ? kStaticScratchBytes : 0,
                              stream);
 }
 

@@ -7,10 +7,8 @@
 
 namespace kvq {
 
-// Longest split-K context partition (tokens); bounds the block-id staging area.
-constexpr int kMaxPartition = 8192;
-// Most split-K partitions per sequence (bounds the merge's shared memory).
-constexpr int kMaxPartitions = 512;
+// Most stream-K ranges (CTAs per head group) of one decode launch.
+constexpr int kMaxCtas = 65535;
 
 struct WriteArgs {
   const uint16_t* key;    // bf16 bits
@@ -42,21 +40,25 @@ struct DecodeArgs {
   const int32_t* block_table;
   const int32_t* context_lens;
   const int8_t* signs;
-  float* ws_acc;  // [S, Hq, NP, D]
-  float* ws_ml;   // [S, Hq, NP, 2]
-  unsigned long long* counters;  // [S, Hkv]: (epoch << 16) | partitions done
-  unsigned long long epoch;      // 48-bit tag of this call
+  float* ws_acc;  // [NC, head groups, 2, heads per group, D]: partial accumulators
+  float* ws_ml;   // [NC, head groups, 2, heads per group, 2]: partial (max, sum)
+  unsigned long long* tags;    // [NC, head groups, 2]: the call's tag once a slot is written
+  unsigned long long* claims;  // [S, head groups]: the call's tag once a merge is claimed
+  unsigned long long epoch;    // nonzero tag of this call
   int num_seqs;
   int num_q_heads;
   int num_kv_heads;
   int gqa;
+  int heads_per_cta;  // kv-heads per CTA (= consumer warps), divides num_kv_heads
+  int one_box;        // K / V tile loaded head-major by one TMA each (else per head)
   int block_size;
   int block_shift;  // log2(block_size)
   int num_blocks;
   int max_blocks_per_seq;
   int max_context_len;
-  int partition_tokens;  // P, multiple of 64
-  int num_partitions;    // NP
+  int num_ctas;          // NC: stream-K ranges (CTAs per head group)
+  int split_h;           // ranges [0, split_h) weigh split_wa, the others split_wb
+  int split_wa, split_wb;
   float qk_scale;        // sm_scale * log2(e) [* k_scale for symmetric K]
   float v_scale;         // symmetric V: multiplies the output
   float cR;

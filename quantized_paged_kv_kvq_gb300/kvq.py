@@ -26,6 +26,7 @@ DEVERR_SLOT_RANGE = 1
 DEVERR_BLOCK_RANGE = 2
 DEVERR_CONTEXT_RANGE = 4
 DEVERR_COMBINE = 8
+DEVERR_TIMEOUT = 16
 
 
 class KvqError(RuntimeError):
@@ -185,18 +186,18 @@ def kvq_write_cache(cache: KVCache, key: torch.Tensor, value: torch.Tensor,
 
 
 def kvq_decode_workspace_size(cache: KVCache, num_seqs: int, num_q_heads: int,
-                              max_context_len: int, partition_tokens: int = 0) -> int:
+                              max_context_len: int, num_ctas: int = 0) -> int:
     lib = load_library()
     n = ctypes.c_size_t(0)
     d = cache.desc()
     st = lib.kvq_decode_workspace_size_ex(ctypes.byref(d), num_seqs, num_q_heads,
-                                          max_context_len, partition_tokens, ctypes.byref(n))
+                                          max_context_len, num_ctas, ctypes.byref(n))
     _check(st, "kvq_decode_workspace_size")
     return int(n.value)
 
 
 def _decode_call(fn_name, cache, query, out, block_table, context_lens, max_context_len,
-                 sm_scale, workspace, partition_tokens, stream):
+                 sm_scale, workspace, num_ctas, stream):
     lib = load_library()
     assert query.dtype == torch.bfloat16 and out.dtype == torch.bfloat16
     assert query.is_contiguous() and out.is_contiguous()
@@ -208,7 +209,7 @@ def _decode_call(fn_name, cache, query, out, block_table, context_lens, max_cont
     st = getattr(lib, fn_name)(ctypes.byref(d), _ptr(cache.k_cache), _ptr(cache.v_cache),
                                _ptr(out), _ptr(query), s, hq, _ptr(block_table),
                                block_table.shape[1], _ptr(context_lens), max_context_len,
-                               float(sm_scale), partition_tokens, _ptr(workspace), ws_bytes,
+                               float(sm_scale), num_ctas, _ptr(workspace), ws_bytes,
                                _stream(stream))
     _check(st, fn_name)
     return out
@@ -217,15 +218,15 @@ def _decode_call(fn_name, cache, query, out, block_table, context_lens, max_cont
 def kvq_paged_decode(cache: KVCache, query: torch.Tensor, out: torch.Tensor,
                      block_table: torch.Tensor, context_lens: torch.Tensor, max_context_len: int,
                      sm_scale: float, workspace: Optional[torch.Tensor] = None,
-                     partition_tokens: int = 0, stream=None) -> torch.Tensor:
+                     num_ctas: int = 0, stream=None) -> torch.Tensor:
     """out[s, h] = softmax(sm_scale q k^T) v over the paged cache (bf16 [S, Hq, D])."""
     return _decode_call("kvq_paged_decode_ex", cache, query, out, block_table, context_lens,
-                        max_context_len, sm_scale, workspace, partition_tokens, stream)
+                        max_context_len, sm_scale, workspace, num_ctas, stream)
 
 
 def kvq_paged_decode_static(cache: KVCache, query: torch.Tensor, out: torch.Tensor,
                             block_table: torch.Tensor, context_lens: torch.Tensor,
-                            max_context_len: int, sm_scale: float, partition_tokens: int = 0,
+                            max_context_len: int, sm_scale: float, num_ctas: int = 0,
                             stream=None) -> torch.Tensor:
     """kvq_paged_decode for callers that cannot allocate: the split-K scratch is
     the library's own fixed array (kvq_paged_decode_static_capacity() bytes)
@@ -240,7 +241,7 @@ def kvq_paged_decode_static(cache: KVCache, query: torch.Tensor, out: torch.Tens
     st = lib.kvq_paged_decode_static(ctypes.byref(d), _ptr(cache.k_cache), _ptr(cache.v_cache),
                                      _ptr(out), _ptr(query), s, hq, _ptr(block_table),
                                      block_table.shape[1], _ptr(context_lens), max_context_len,
-                                     float(sm_scale), partition_tokens, _stream(stream))
+                                     float(sm_scale), num_ctas, _stream(stream))
     _check(st, "kvq_paged_decode_static")
     return out
 

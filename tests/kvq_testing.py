@@ -58,16 +58,16 @@ class GpuRun:
     def write(self):
         kvq.kvq_write_cache(self.cache, self.key, self.value, self.slots)
 
-    def decode(self, partition_tokens: int = 0, sm_scale=None, out=None) -> torch.Tensor:
+    def decode(self, num_ctas: int = 0, sm_scale=None, out=None) -> torch.Tensor:
         wl = self.wl
         sm = float(OA.default_sm_scale(wl.head_dim)) if sm_scale is None else sm_scale
         nbytes = kvq.kvq_decode_workspace_size(self.cache, wl.num_seqs, wl.num_q_heads,
-                                               wl.max_context_len, partition_tokens)
+                                               wl.max_context_len, num_ctas)
         ws = torch.empty(max(nbytes, 16) // 4 + 4, dtype=torch.float32, device=self.query.device)
         if out is None:
             out = torch.empty_like(self.query)
         kvq.kvq_paged_decode(self.cache, self.query, out, self.block_table, self.context_lens,
-                             wl.max_context_len, sm, ws, partition_tokens)
+                             wl.max_context_len, sm, ws, num_ctas)
         return out
 
     def cache_numpy(self):

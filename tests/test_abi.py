@@ -97,19 +97,24 @@ def test_decode_validation(lib):
     d = _desc()
     assert _decode(lib, d, hq=30) == 1  # not a multiple of the kv heads
     assert _decode(lib, d, hq=8 * 16) == 2  # GQA ratio above 8
-    assert _decode(lib, d, p=100) == 1  # partition not a multiple of 64
+    assert _decode(lib, d, p=-1) == 1  # negative CTA count
+    assert _decode(lib, d, p=70000) == 1  # more CTAs than a grid dimension holds
     assert _decode(lib, d, mb=10) == 1  # block table shorter than max context
     assert _decode(lib, d, q=None) == 1
+    assert _decode(lib, d, q=FAKE + 2) == 1  # query rows are fetched in 16-byte pieces
+    assert _decode(lib, d, out=FAKE + 8) == 1  # outputs are stored in 16-byte pieces
     assert _decode(lib, d, sm=float("inf")) == 1
-    assert _decode(lib, d) == 3  # needs a workspace (4 partitions)
+    assert _decode(lib, d) == 3  # needs a workspace (256 CTAs)
     assert _decode(lib, d, ws=FAKE, wsb=10) == 3
     n = ctypes.c_size_t(0)
     assert lib.kvq_decode_workspace_size_ex(ctypes.byref(d), 4, 32, 1024, 256,
                                             ctypes.byref(n)) == 0
-    assert n.value == 4 * 32 * 4 * (128 + 2) * 4 + 4 * 8 * 8  # partials + counters
-    assert lib.kvq_decode_workspace_size_ex(ctypes.byref(d), 4, 32, 200, 256,
+    # two partial slots per CTA and head, two completion tags per CTA and a merge
+    # claim per sequence (one head group)
+    assert n.value == 256 * 2 * 32 * (128 + 2) * 4 + 256 * 1 * 2 * 8 + 4 * 1 * 8
+    assert lib.kvq_decode_workspace_size_ex(ctypes.byref(d), 4, 32, 200, 1,
                                             ctypes.byref(n)) == 0
-    assert n.value == 0  # one partition: no workspace
+    assert n.value == 0  # one CTA: every sequence is whole, no workspace
     assert _decode(lib, d, s=0) == 0
 
 
