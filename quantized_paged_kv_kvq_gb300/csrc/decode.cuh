@@ -162,8 +162,9 @@ __device__ __forceinline__ void v_pair(uint32_t wa, uint32_t wb, int i, uint32_t
     } else if constexpr (VF == E5M2) {
       rg = prmt(il, 0u, 0x1404);
       rg8 = prmt(il, 0u, 0x3424);
-    } else {
-      constexpr uint32_t bias = VF == INT8 ? 0x64806480u : 0x64006400u;  // 1152 / 1024
+    } else {  // exact: subtract the 1152 / 1024 offset in fp16 (a large offset left in
+              // the fp32 sum costs accuracy over long contexts)
+      constexpr uint32_t bias = VF == INT8 ? 0x64806480u : 0x64006400u;
       rg = hsub2_u32(prmt(il, K64, 0x4140), bias);
       rg8 = hsub2_u32(prmt(il, K64, 0x4342), bias);
     }
@@ -376,15 +377,19 @@ __device__ __forceinline__ long long range_start(const DecodeArgs& a, long long 
                        static_cast<long long>(a.split_wb) * (a.num_ctas - a.split_h);
   return T * wk / wt;
 }
-// The range holding global tile x < T: the largest k with range_start(k) <= x.
+// The range holding global tile x < T: the largest k with range_start(k) <= x
+// (the inverse of range_start on each of its two linear pieces).
 __device__ __forceinline__ int range_of(const DecodeArgs& a, long long x, long long T) {
-  int lo = 0, hi = a.num_ctas - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (range_start(a, T, mid) <= x) lo = mid;
-    else hi = mid - 1;
+  const int nc = a.num_ctas, hh = a.split_h;
+  const long long wt = static_cast<long long>(a.split_wa) * hh +
+                       static_cast<long long>(a.split_wb) * (nc - hh);
+  long long k;
+  if (hh >= nc || x < range_start(a, T, hh)) {
+    k = ((x + 1) * wt - 1) / (T * a.split_wa);
+  } else {
+    k = hh + ((x + 1) * wt - T * a.split_wa * hh - 1) / (T * a.split_wb);
   }
-  return lo;
+  return static_cast<int>(k < 0 ? 0 : k >= nc ? nc - 1 : k);
 }
 
 template <int N>
@@ -445,53 +450,56 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long 
   for (int n0 = 0; n0 < G; n0 += 32 / LQ) {  // every lane runs every pass (shuffles below)
     const int nn = n0 + lane / LQ;
     const bool act = nn < G;
-    // slot row of range ka + p for query head nn, or -1 if the range is empty
-    auto slot_of = [&](int p) -> long long {
-      if (!act || p >= np) return -1;
-      const int kk = ka + p;
-      const long long r0 = range_start(a, T, kk), r1 = range_start(a, T, kk + 1);
-      if (r0 >= r1) return -1;
-      const int jj = (r0 >= ps) ? 0 : 1;
-      return ((static_cast<long long>(kk) * HG + hg) * 2 + jj) * rows + warp * G + nn;
-    };
     float M = -INFINITY, Lsum = 0.f;
     float acc[DL];
 #pragma unroll
     for (int e = 0; e < DL; ++e) acc[e] = 0.f;
 #pragma unroll 1
-    for (int p0 = 0; p0 < np; p0 += PU) {
-      float ml[PU][2], v[PU][DL];
+    for (int c0 = 0; c0 < np; c0 += 32) {  // ranges ka+c0 .. ka+c0+31
+      // lane p: first slot row of range ka + c0 + p, or -1 if that range is empty
+      int base = -1;
+      if (c0 + lane < np) {
+        const int kk = ka + c0 + lane;
+        const long long r0 = range_start(a, T, kk), r1 = range_start(a, T, kk + 1);
+        if (r0 < r1) base = ((kk * HG + hg) * 2 + (r0 >= ps ? 0 : 1)) * rows;
+      }
+      const int cn = min(32, np - c0);
+#pragma unroll 1
+      for (int p0 = 0; p0 < cn; p0 += PU) {
+        float ml[PU][2], v[PU][DL];
 #pragma unroll
-      for (int u = 0; u < PU; ++u) {
-        const long long sl = slot_of(p0 + u);
-        if (sl >= 0) {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + 2 * sl));
-          ml[u][0] = x.x;
-          ml[u][1] = x.y;
-          ldcg_vec<DL>(a.ws_acc + sl * D + r * DL, v[u]);
-        } else {
-          ml[u][0] = -INFINITY;
-          ml[u][1] = 0.f;
+        for (int u = 0; u < PU; ++u) {
+          const int b = __shfl_sync(0xffffffffu, base, (p0 + u) & 31);
+          if (act && p0 + u < cn && b >= 0) {
+            const long long sl = static_cast<long long>(b) + warp * G + nn;
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + 2 * sl));
+            ml[u][0] = x.x;
+            ml[u][1] = x.y;
+            ldcg_vec<DL>(a.ws_acc + sl * D + r * DL, v[u]);
+          } else {
+            ml[u][0] = -INFINITY;
+            ml[u][1] = 0.f;
 #pragma unroll
-          for (int e = 0; e < DL; ++e) v[u][e] = 0.f;
+            for (int e = 0; e < DL; ++e) v[u][e] = 0.f;
+          }
         }
-      }
-      float bm = ml[0][0];
+        float bm = ml[0][0];
 #pragma unroll
-      for (int u = 1; u < PU; ++u) bm = fmaxf(bm, ml[u][0]);
-      if (bm > M) {  // raise the running maximum, rescaling what was summed so far
-        const float sc = fast_exp2(M - bm);
-        Lsum *= sc;
+        for (int u = 1; u < PU; ++u) bm = fmaxf(bm, ml[u][0]);
+        if (bm > M) {  // raise the running maximum, rescaling what was summed so far
+          const float sc = fast_exp2(M - bm);
+          Lsum *= sc;
 #pragma unroll
-        for (int e = 0; e < DL; ++e) acc[e] *= sc;
-        M = bm;
-      }
+          for (int e = 0; e < DL; ++e) acc[e] *= sc;
+          M = bm;
+        }
 #pragma unroll
-      for (int u = 0; u < PU; ++u) {
-        const float w = fast_exp2(ml[u][0] - M);
-        Lsum += w * ml[u][1];
+        for (int u = 0; u < PU; ++u) {
+          const float w = fast_exp2(ml[u][0] - M);
+          Lsum += w * ml[u][1];
 #pragma unroll
-        for (int e = 0; e < DL; ++e) acc[e] += w * v[u][e];
+          for (int e = 0; e < DL; ++e) acc[e] += w * v[u][e];
+        }
       }
     }
     const float il = act ? 1.0f / Lsum : 0.f;
