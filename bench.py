@@ -2,13 +2,12 @@
 """Benchmark of the quantized paged KV cache hot path on GB300.
 
 One step = the whole path on one batch of synthetic input: quantize-and-
-scatter every context token into the paged cache (kvq_write_cache), then
-single-token paged decode over it (kvq_paged_decode, its partition and
-one launch; the last CTA of each (sequence, kv-head) merges the
-split-K partitions).  Inputs are resident in HBM before the
-timed region; L2 is flushed (a 2x-L2 memset, then a 2x-L2 read) before every
-timed kernel group,
-outside the CUDA-event pairs.  One JSON line on stdout (rank 0).
+scatter every context token into the paged cache (kvq_write_cache, one
+launch), then single-token paged decode over it (kvq_paged_decode, one
+stream-K launch that also merges sequences split between CTAs).  Inputs are
+resident in HBM before the timed region; L2 is flushed (a 2x-L2 memset, then a
+2x-L2 read) before each of the two kernels, outside the CUDA-event pairs.
+One JSON line on stdout (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle, as the reference arm
@@ -36,6 +35,7 @@ METRIC = "quantized paged decode: effective KV GB/s vs HBM peak; decode & cache-
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SOURCES = ["decode.cuh", "decode_launch.cuh", "kvq_device.cuh", "decode_d128_sym.cu",
                   "decode_d128_asym.cu", "decode_d64_sym.cu", "decode_d64_asym.cu"]
+WRITE_SOURCES = ["write.cu", "kvq_device.cuh"]
 
 
 def parse_args(argv=None):
@@ -80,12 +80,16 @@ def write_bytes(wl) -> int:
     return t * (2 * wl.num_kv_heads * wl.head_dim * 2 + kv_bytes_per_token(wl) + 8)
 
 
-def decode_source_hash() -> str:
+def source_hash(names) -> str:
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "quantized_paged_kv_kvq_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def decode_source_hash() -> str:
+    return source_hash(DECODE_SOURCES)
 
 
 def measured_peaks():
@@ -98,10 +102,11 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the partition kernel from the committed ncu
-    summary, if it was taken on the current decode sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_partition_{workload}.md")
+def profiled_traffic(workload: str, kernel: str = "decode_partition"):
+    """DRAM bytes per launch of a kernel from its committed ncu summary
+    (profiles/<kernel>_<workload>.md), if that was taken on the current
+    sources of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -110,7 +115,11 @@ def profiled_traffic(workload: str):
             if ":" in line and line.strip().startswith("- "):
                 k, v = line.strip()[2:].split(":", 1)
                 vals[k.strip()] = v.strip().strip("`")
-    if vals.get("decode_source_sha256_16") != decode_source_hash():
+    if kernel == "decode_partition":
+        ok = vals.get("decode_source_sha256_16") == decode_source_hash()
+    else:
+        ok = vals.get("write_source_sha256_16") == source_hash(WRITE_SOURCES)
+    if not ok:
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -318,6 +327,16 @@ def aggregate(per_rank_times, per_rank_units):
     return (sum(per_rank_units) / t) if t > 0 else float("nan")
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats over all ranks (identity at N=1)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def run_kvq(args, rank: int, world: int, local_rank: int):
     import numpy as np
     import torch
@@ -401,17 +420,26 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
         dist.barrier()
     wall = time.perf_counter() - w0
     clocks = sampler.stop()
-    t_write = sum(e[0].elapsed_time(e[1]) for e in events) / 1e3
-    t_dec = sum(e[2].elapsed_time(e[3]) for e in events) / 1e3
-    times = torch.tensor([t_write, t_dec, wall], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_write, t_dec, wall = times.tolist()
+    w_ms = np.array([e[0].elapsed_time(e[1]) for e in events])
+    d_ms = np.array([e[2].elapsed_time(e[3]) for e in events])
+    t_write, t_dec = float(w_ms.sum()) / 1e3, float(d_ms.sum()) / 1e3
+    pct = lambda x: {f"p{q}": round(float(np.percentile(x, q)) * 1e3, 3) for q in (10, 50, 90)}
+    t_write, t_dec, wall = max_over_ranks([t_write, t_dec, wall], dev)
     dbytes, wbytes = decode_bytes(wl), write_bytes(wl)
     K = args.steps
     gbs = aggregate([t_dec], [world * dbytes * K]) / 1e9
     hbm, peak_src = measured_peaks()
     achieved = dbytes / (t_dec / K) / 1e9
+    achieved_w = wbytes / (t_write / K) / 1e9
+    peak_note = f"{peak_src} hbm_gbs (burst copy)"
+    rl_decode = {"bound": "hbm", "kernel": "decode_partition_kernel", "achieved": achieved,
+                 "peak": hbm, "peak_source": peak_note, "unit": "GB/s", "frac": achieved / hbm,
+                 "traffic": profiled_traffic(args.workload, "decode_partition"),
+                 "algorithmic_bytes": dbytes}
+    rl_write = {"bound": "hbm", "kernel": "write_cache_kernel", "achieved": achieved_w,
+                "peak": hbm, "peak_source": peak_note, "unit": "GB/s", "frac": achieved_w / hbm,
+                "traffic": profiled_traffic(args.workload, "write_cache"),
+                "algorithmic_bytes": wbytes}
 
     # end to end through the public API: pinned host inputs in, result out
     e2e = None
@@ -439,13 +467,11 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
             e2e_step()
         e1.record()
         torch.cuda.synchronize()
-        t_e2e = torch.tensor([e0.elapsed_time(e1) / 1e3], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
+        t_e2e = max_over_ranks([e0.elapsed_time(e1) / 1e3], dev)[0]
         h2d = sum(x.numel() * x.element_size() for x in h_in)
-        e2e = {"value": world * dbytes * n_e2e / t_e2e.item() / 1e9, "unit": "GB/s",
+        e2e = {"value": world * dbytes * n_e2e / t_e2e / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h_out.numel() * 2,
-               "steps": n_e2e, "ms_per_step": 1e3 * t_e2e.item() / n_e2e}
+               "steps": n_e2e, "ms_per_step": 1e3 * t_e2e / n_e2e}
 
     if world > 1:
         dist.barrier()
@@ -468,17 +494,18 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
                    "decode_ctas": P or "auto", "l2": "flushed before the write and before the decode (2xL2 memset, "
                    "then a 2xL2 read), outside the timed events"},
         "decode_tok_s": world * wl.num_seqs * K / t_dec,
-        "decode_us": 1e6 * t_dec / K, "decode_partitions": ws_bytes > 0,
+        "decode_us": 1e6 * t_dec / K, "decode_us_pct": pct(d_ms),
+        "decode_split": ws_bytes > 0,
         "cache_write_tok_s": world * wl.num_tokens * K / t_write,
         "cache_write_gbs": world * wbytes * K / t_write / 1e9,
-        "cache_write_us": 1e6 * t_write / K,
+        "cache_write_us": 1e6 * t_write / K, "cache_write_us_pct": pct(w_ms),
         "cache_write_frac_of_hbm": (wbytes * K / t_write / 1e9) / hbm,
         "decode_bytes": dbytes, "write_bytes": wbytes,
         "wall_s_timed_region": wall,
-        "roofline": {"bound": "hbm", "kernel": "decode_partition_kernel", "achieved": achieved,
-                     "peak": hbm, "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-                     "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": profiled_traffic(args.workload)},
+        # the dominant kernel of the step (largest share of its time) first
+        "roofline": rl_write if t_write >= t_dec else rl_decode,
+        "roofline_decode": rl_decode,
+        "roofline_write": rl_write,
         "decode_frac_of_hbm": gbs / world / hbm,
         "e2e": e2e,
         "gpu_launches": launches,

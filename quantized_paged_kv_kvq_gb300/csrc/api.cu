@@ -91,14 +91,14 @@ size_t workspace_bytes_for(int num_seqs, int hq, int hkv, int d, int nc) {
 }
 
 // Stream-K range weights.  With one head group and two CTAs per SM, the CTA
-// an SM receives first runs about 15% faster than the second (the warp
-// schedulers favour the older CTA's warps; measured on GB300 with per-CTA
-// timers), so the first-wave ranges are made longer in that proportion.
+// an SM receives first gets about 55% of the SM's throughput while both run
+// (the warp schedulers favour the older CTA's warps; measured on GB300 with
+// per-CTA timers), so the first-wave ranges are made longer in proportion.
 void range_weights(int nc, int head_groups, int sms, DecodeArgs* a) {
   if (head_groups == 1 && sms > 0 && nc == 2 * sms) {
     a->split_h = sms;
-    a->split_wa = 107;
-    a->split_wb = 93;
+    a->split_wa = 111;
+    a->split_wb = 89;
   } else {
     a->split_h = nc;
     a->split_wa = a->split_wb = 1;

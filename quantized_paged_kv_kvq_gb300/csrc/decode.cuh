@@ -240,13 +240,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+// 4-D TMA tile load completing on mbarrier `bar`, with an L2 eviction policy
+// (the cache stream is read once: evict-first keeps it from flushing the
+// small data that is read again -- partial results, queries, block tables).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, int w, uint32_t bar) {
+                                            int z, int w, uint32_t bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
       : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 // Shared address of 16-byte chunk `chunk` (plus `byte` within it) of row `row`
 // of a swizzled box starting at `base` (1024-byte aligned for swizzled boxes).
@@ -413,27 +421,24 @@ __device__ __forceinline__ void store_f32_run(float* dst, const float (&v)[N]) {
     reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
+// N floats of a row at p[32i + e] (i < N/4, e < 4): one 16-byte load per i.
 template <int N>
-__device__ __forceinline__ void ldcg_vec(const float* p, float (&v)[N]) {
-  if constexpr (N % 4 == 0) {
+__device__ __forceinline__ void ldcg_interleaved(const float* p, float (&v)[N]) {
+  static_assert(N % 4 == 0, "whole 16-byte pieces");
 #pragma unroll
-    for (int i = 0; i < N / 4; ++i) {
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(p) + i);
-      v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
-    }
-  } else {
-    static_assert(N == 2, "vector width");
-    const float2 x = __ldcg(reinterpret_cast<const float2*>(p));
-    v[0] = x.x; v[1] = x.y;
+  for (int i = 0; i < N / 4; ++i) {
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(p + 32 * i));
+    v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
   }
 }
 
 // Log-sum-exp merge of the partial results of sequence s (tiles [ps, ps+tiles)
 // of the global order) held in the slots of stream-K ranges ka..kb, by one warp
 // for its kv-head's G query heads, four at a time: lane (nn, r) owns query head
-// nn's dims r*DL .. r*DL+DL-1.  Every lane reads every range's (m, l) itself;
-// the loads of PU ranges are issued together and merged with a running
-// maximum, so a merge costs a few L2 round trips whatever the number of ranges.
+// nn's dims 32i + 4r + e (i < DL/4, e < 4), so each 16-byte load instruction
+// of the warp reads whole 128-byte lines.  Every lane reads every range's
+// (m, l) itself; the loads of PU ranges are issued together and merged with a
+// running maximum, so a merge costs a few L2 round trips.
 template <int D, bool KVARN>
 __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long long ps, int tiles,
                                                long long T, int NC, int HG, int hg, int warp,
@@ -475,7 +480,7 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long 
             const float2 x = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + 2 * sl));
             ml[u][0] = x.x;
             ml[u][1] = x.y;
-            ldcg_vec<DL>(a.ws_acc + sl * D + r * DL, v[u]);
+            ldcg_interleaved<DL>(a.ws_acc + sl * D + 4 * r, v[u]);
           } else {
             ml[u][0] = -INFINITY;
             ml[u][1] = 0.f;
@@ -505,19 +510,26 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long 
     const float il = act ? 1.0f / Lsum : 0.f;
 #pragma unroll
     for (int e = 0; e < DL; ++e) acc[e] *= il;
-    if constexpr (KVARN) {  // inverse rotation x = d . (cR * H y) across the LQ lanes
+    if constexpr (KVARN) {  // inverse rotation x = d . (cR * H y): the Walsh-Hadamard
+      // matrix is unchanged by a permutation of index bits, so the butterflies run
+      // over the local index (dim bits 0-1, 5-6) and then across the lanes (2-4)
       fwht_lanes<DL, LQ>(acc, r);
 #pragma unroll
       for (int e = 0; e < DL; ++e) {
-        const int dd = r * DL + e;
+        const int dd = 32 * (e >> 2) + 4 * r + (e & 3);
         const float sgn = (a.signs != nullptr && a.signs[dd] < 0) ? -1.f : 1.f;
         acc[e] = __fmul_rn(acc[e], a.cR) * sgn;
       }
     }
     if (act) {
-      uint16_t* orow = a.out + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G + nn) * D + r * DL;
+      uint16_t* orow = a.out + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G + nn) * D + 4 * r;
 #pragma unroll
-      for (int e = 0; e < DL; ++e) orow[e] = f2bf(acc[e]);
+      for (int i = 0; i < DL / 4; ++i) {
+        uint2 w;
+        w.x = static_cast<uint32_t>(f2bf(acc[4 * i])) | (static_cast<uint32_t>(f2bf(acc[4 * i + 1])) << 16);
+        w.y = static_cast<uint32_t>(f2bf(acc[4 * i + 2])) | (static_cast<uint32_t>(f2bf(acc[4 * i + 3])) << 16);
+        *reinterpret_cast<uint2*>(orow + 32 * i) = w;
+      }
     }
   }
 }
@@ -700,6 +712,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     *cur = u;
   }
   auto issue = [&](int st) {  // the cursor's tile into stage st, then advance the cursor
+    const uint64_t pol = l2_evict_first_policy();
     Cursor u = *cur;
     TileHeader& hd = hdr[st];
     hd.s = u.s;
@@ -720,16 +733,16 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     const uint32_t bar = full_s + 8 * st;
     mbar_arrive_expect(bar, tile_bytes);
     if (a.one_box) {
-      tma_load_4d(sb, &maps.k, 0, off, hg * hpc, blk, bar);
-      tma_load_4d(sb + v_off, &maps.v, 0, off, hg * hpc, blk, bar);
+      tma_load_4d(sb, &maps.k, 0, off, hg * hpc, blk, bar, pol);
+      tma_load_4d(sb + v_off, &maps.v, 0, off, hg * hpc, blk, bar, pol);
     } else {
       for (int hh = 0; hh < hpc; ++hh) {
-        tma_load_4d(sb + hh * C::K_HEAD, &maps.k, 0, hg * hpc + hh, off, blk, bar);
-        tma_load_4d(sb + v_off + hh * C::V_HEAD, &maps.v, 0, hg * hpc + hh, off, blk, bar);
+        tma_load_4d(sb + hh * C::K_HEAD, &maps.k, 0, hg * hpc + hh, off, blk, bar, pol);
+        tma_load_4d(sb + v_off + hh * C::V_HEAD, &maps.v, 0, hg * hpc + hh, off, blk, bar, pol);
       }
     }
-    if constexpr (C::KMF > 0) tma_load_4d(sb + m_off, &maps.km, off, 0, hg * hpc, blk, bar);
-    if constexpr (C::VMF > 0) tma_load_4d(sb + vm_off, &maps.vm, off, 0, hg * hpc, blk, bar);
+    if constexpr (C::KMF > 0) tma_load_4d(sb + m_off, &maps.km, off, 0, hg * hpc, blk, bar, pol);
+    if constexpr (C::VMF > 0) tma_load_4d(sb + vm_off, &maps.vm, off, 0, hg * hpc, blk, bar, pol);
     ++u.i;
     if (++u.t == u.tiles && u.i < n) {  // on to the next sequence with tokens
       u.ps += u.tiles;
