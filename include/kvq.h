@@ -129,7 +129,8 @@ kvq_status kvq_write_cache(const kvq_cache_desc* cache, void* k_cache, void* v_c
 /*
  * kvq_decode_workspace_size -- bytes of device workspace kvq_paged_decode
  * needs for these sizes: partial results of sequences split between CTAs
- * (num_ctas * 2 * num_q_heads * (head_dim + 2) * 4 bytes, 0 with one CTA)
+ * (num_ctas * 2 * num_q_heads * (head_dim * 2 + 8) bytes: fp16 outputs and
+ * fp32 (max, sum); 0 with one CTA)
  * two 8-byte completion tags per (CTA, group of 8 kv-heads) and one 8-byte
  * merge claim per (sequence, group of 8 kv-heads).  Depends on the device's
  * SM count (current device).

@@ -79,30 +79,15 @@ int auto_ctas(int num_seqs, int max_ctx, int head_groups, int sms) {
 }
 
 // Workspace: per (range, head group, first/last segment of the range, head) a
-// partial accumulator of D f32 and its (max, sum); per (range, head group,
-// first/last segment) a 64-bit completion tag; per (sequence, head group) a
-// 64-bit merge claim.  One range needs none.
+// partial output of D fp16 (acc / l) and its (max, sum) in f32; per (range,
+// head group, first/last segment) a 64-bit completion tag; per (sequence, head
+// group) a 64-bit merge claim.  One range needs none.
 size_t workspace_bytes_for(int num_seqs, int hq, int hkv, int d, int nc) {
   if (nc <= 1) return 0;
   const size_t rows = static_cast<size_t>(nc) * 2 * hq;
   const size_t groups = static_cast<size_t>(hkv / heads_per_cta(hkv));
-  return rows * (d + 2) * sizeof(float) + static_cast<size_t>(nc) * groups * 2 * 8 +
+  return rows * (d * 2 + 2 * sizeof(float)) + static_cast<size_t>(nc) * groups * 2 * 8 +
          static_cast<size_t>(num_seqs) * groups * 8;
-}
-
-// Stream-K range weights.  With one head group and two CTAs per SM, the CTA
-// an SM receives first gets about 55% of the SM's throughput while both run
-// (the warp schedulers favour the older CTA's warps; measured on GB300 with
-// per-CTA timers), so the first-wave ranges are made longer in proportion.
-void range_weights(int nc, int head_groups, int sms, DecodeArgs* a) {
-  if (head_groups == 1 && sms > 0 && nc == 2 * sms) {
-    a->split_h = sms;
-    a->split_wa = 111;
-    a->split_wb = 89;
-  } else {
-    a->split_h = nc;
-    a->split_wa = a->split_wb = 1;
-  }
 }
 
 // Nonzero 64-bit tag, different for every decode call of the process, so that
@@ -250,8 +235,9 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
   a.context_lens = context_lens;
   a.signs = cache->signs;
   const size_t rows = static_cast<size_t>(NC) * 2 * num_q_heads;
-  a.ws_acc = need ? static_cast<float*>(workspace) : nullptr;
-  a.ws_ml = need ? static_cast<float*>(workspace) + rows * cache->head_dim : nullptr;
+  a.ws_acc = need ? static_cast<__half*>(workspace) : nullptr;
+  a.ws_ml = need ? reinterpret_cast<float*>(static_cast<__half*>(workspace) + rows * cache->head_dim)
+                 : nullptr;
   a.tags = need ? reinterpret_cast<unsigned long long*>(a.ws_ml + rows * 2) : nullptr;
   a.claims = need ? a.tags + static_cast<size_t>(NC) * (cache->num_kv_heads / heads_per_cta(cache->num_kv_heads)) * 2
                   : nullptr;
@@ -267,7 +253,6 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.max_context_len = max_context_len;
   a.num_ctas = NC;
-  range_weights(NC, cache->num_kv_heads / heads_per_cta(cache->num_kv_heads), sm_count(), &a);
   a.qk_scale = sm_scale * kLog2e * (is_asym(cache->k_fmt) ? 1.0f : cache->k_scale);
   a.v_scale = is_asym(cache->v_fmt) ? 1.0f : cache->v_scale;
   a.cR = rotation_scale(cache->head_dim);

@@ -375,29 +375,13 @@ __device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int s) {
   return ctx <= 0 ? 0 : (min(ctx, a.max_context_len) + 15) >> 4;
 }
 
-// First global tile of stream-K range k (range NC starts at T).  Ranges are cut
-// in proportion to weights: split_wa for the first split_h ranges, split_wb
-// for the rest.
+// First global tile of stream-K range k: ranges [k*T/NC, (k+1)*T/NC).
 __device__ __forceinline__ long long range_start(const DecodeArgs& a, long long T, int k) {
-  const long long wk = static_cast<long long>(a.split_wa) * min(k, a.split_h) +
-                       static_cast<long long>(a.split_wb) * max(k - a.split_h, 0);
-  const long long wt = static_cast<long long>(a.split_wa) * a.split_h +
-                       static_cast<long long>(a.split_wb) * (a.num_ctas - a.split_h);
-  return T * wk / wt;
+  return T * k / a.num_ctas;
 }
-// The range holding global tile x < T: the largest k with range_start(k) <= x
-// (the inverse of range_start on each of its two linear pieces).
+// The range holding global tile x < T: the largest k with range_start(k) <= x.
 __device__ __forceinline__ int range_of(const DecodeArgs& a, long long x, long long T) {
-  const int nc = a.num_ctas, hh = a.split_h;
-  const long long wt = static_cast<long long>(a.split_wa) * hh +
-                       static_cast<long long>(a.split_wb) * (nc - hh);
-  long long k;
-  if (hh >= nc || x < range_start(a, T, hh)) {
-    k = ((x + 1) * wt - 1) / (T * a.split_wa);
-  } else {
-    k = hh + ((x + 1) * wt - T * a.split_wa * hh - 1) / (T * a.split_wb);
-  }
-  return static_cast<int>(k < 0 ? 0 : k >= nc ? nc - 1 : k);
+  return static_cast<int>(((x + 1) * a.num_ctas - 1) / T);
 }
 
 template <int N>
@@ -414,38 +398,42 @@ __device__ __forceinline__ void store_bf16_run(uint16_t* dst, const float (&v)[N
   }
 }
 template <int N>
-__device__ __forceinline__ void store_f32_run(float* dst, const float (&v)[N]) {
-  static_assert(N % 4 == 0, "run of 16-byte pieces");
+__device__ __forceinline__ void store_f16_run(__half* dst, const float (&v)[N]) {
+  static_assert(N % 8 == 0, "run of 16-byte pieces");
 #pragma unroll
-  for (int i = 0; i < N / 4; ++i)
-    reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  for (int i = 0; i < N / 8; ++i)
+    reinterpret_cast<uint4*>(dst)[i] =
+        make_uint4(pack_half2(v[8 * i], v[8 * i + 1]), pack_half2(v[8 * i + 2], v[8 * i + 3]),
+                   pack_half2(v[8 * i + 4], v[8 * i + 5]), pack_half2(v[8 * i + 6], v[8 * i + 7]));
 }
 
-// N floats of a row at p[32i + e] (i < N/4, e < 4): one 16-byte load per i.
+// N fp16 values of a row at p[64i + e] (i < N/8, e < 8): one 16-byte load per i.
 template <int N>
-__device__ __forceinline__ void ldcg_interleaved(const float* p, float (&v)[N]) {
-  static_assert(N % 4 == 0, "whole 16-byte pieces");
+__device__ __forceinline__ void ldcg_halves(const __half* p, uint4 (&v)[N / 8]) {
+  static_assert(N % 8 == 0, "whole 16-byte pieces");
 #pragma unroll
-  for (int i = 0; i < N / 4; ++i) {
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(p + 32 * i));
-    v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
-  }
+  for (int i = 0; i < N / 8; ++i) v[i] = __ldcg(reinterpret_cast<const uint4*>(p + 64 * i));
+}
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
 // Log-sum-exp merge of the partial results of sequence s (tiles [ps, ps+tiles)
 // of the global order) held in the slots of stream-K ranges ka..kb, by one warp
-// for its kv-head's G query heads, four at a time: lane (nn, r) owns query head
-// nn's dims 32i + 4r + e (i < DL/4, e < 4), so each 16-byte load instruction
-// of the warp reads whole 128-byte lines.  Every lane reads every range's
-// (m, l) itself; the loads of PU ranges are issued together and merged with a
-// running maximum, so a merge costs a few L2 round trips.
+// for its kv-head's G query heads, four at a time.  A slot holds, per query
+// head, the range's normalised output acc/l in fp16 and (m, l) in fp32, and
+// out = sum_i 2^(m_i - M) l_i (acc_i / l_i) / sum_i 2^(m_i - M) l_i.  Lane
+// (nn, r) owns query head nn's dims 64i + 8r + e (i < DL/8, e < 8), so each
+// 16-byte load instruction of the warp reads whole 128-byte lines.  Every lane
+// reads every range's (m, l) itself; the loads of PU ranges are issued
+// together and merged with a running maximum: a few L2 round trips per merge.
 template <int D, bool KVARN>
 __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long long ps, int tiles,
                                                long long T, int NC, int HG, int hg, int warp,
                                                int lane, int hpc) {
   constexpr int LQ = 8;                     // lanes per query head
   constexpr int DL = D / LQ;                // dims per lane
-  constexpr int PU = 64 / DL < 8 ? 64 / DL : 8;  // ranges per batch of loads
+  constexpr int PU = 4;        // ranges per batch of loads
   const int G = a.gqa, rows = hpc * G;
   const int r = lane % LQ;
   const int ka = range_of(a, ps, T), kb = range_of(a, ps + tiles - 1, T);
@@ -471,7 +459,8 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long 
       const int cn = min(32, np - c0);
 #pragma unroll 1
       for (int p0 = 0; p0 < cn; p0 += PU) {
-        float ml[PU][2], v[PU][DL];
+        float ml[PU][2];
+        uint4 v[PU][DL / 8];
 #pragma unroll
         for (int u = 0; u < PU; ++u) {
           const int b = __shfl_sync(0xffffffffu, base, (p0 + u) & 31);
@@ -480,12 +469,12 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long 
             const float2 x = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + 2 * sl));
             ml[u][0] = x.x;
             ml[u][1] = x.y;
-            ldcg_interleaved<DL>(a.ws_acc + sl * D + 4 * r, v[u]);
+            ldcg_halves<DL>(a.ws_acc + sl * D + 8 * r, v[u]);
           } else {
             ml[u][0] = -INFINITY;
             ml[u][1] = 0.f;
 #pragma unroll
-            for (int e = 0; e < DL; ++e) v[u][e] = 0.f;
+            for (int i = 0; i < DL / 8; ++i) v[u][i] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         float bm = ml[0][0];
@@ -500,10 +489,18 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long 
         }
 #pragma unroll
         for (int u = 0; u < PU; ++u) {
-          const float w = fast_exp2(ml[u][0] - M);
-          Lsum += w * ml[u][1];
+          const float w = fast_exp2(ml[u][0] - M) * ml[u][1];  // 2^(m - M) l
+          Lsum += w;
 #pragma unroll
-          for (int e = 0; e < DL; ++e) acc[e] += w * v[u][e];
+          for (int i = 0; i < DL / 8; ++i) {
+            const uint32_t q[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float2 f = half2_bits_to_float2(q[t]);
+              acc[8 * i + 2 * t] += w * f.x;
+              acc[8 * i + 2 * t + 1] += w * f.y;
+            }
+          }
         }
       }
     }
@@ -512,23 +509,23 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long 
     for (int e = 0; e < DL; ++e) acc[e] *= il;
     if constexpr (KVARN) {  // inverse rotation x = d . (cR * H y): the Walsh-Hadamard
       // matrix is unchanged by a permutation of index bits, so the butterflies run
-      // over the local index (dim bits 0-1, 5-6) and then across the lanes (2-4)
+      // over the local index (dim bits 0-2, 6) and then across the lanes (3-5)
       fwht_lanes<DL, LQ>(acc, r);
 #pragma unroll
       for (int e = 0; e < DL; ++e) {
-        const int dd = 32 * (e >> 2) + 4 * r + (e & 3);
+        const int dd = 64 * (e >> 3) + 8 * r + (e & 7);
         const float sgn = (a.signs != nullptr && a.signs[dd] < 0) ? -1.f : 1.f;
         acc[e] = __fmul_rn(acc[e], a.cR) * sgn;
       }
     }
     if (act) {
-      uint16_t* orow = a.out + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G + nn) * D + 4 * r;
+      uint16_t* orow = a.out + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G + nn) * D + 8 * r;
 #pragma unroll
-      for (int i = 0; i < DL / 4; ++i) {
-        uint2 w;
-        w.x = static_cast<uint32_t>(f2bf(acc[4 * i])) | (static_cast<uint32_t>(f2bf(acc[4 * i + 1])) << 16);
-        w.y = static_cast<uint32_t>(f2bf(acc[4 * i + 2])) | (static_cast<uint32_t>(f2bf(acc[4 * i + 3])) << 16);
-        *reinterpret_cast<uint2*>(orow + 32 * i) = w;
+      for (int i = 0; i < DL / 8; ++i) {
+        float piece[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) piece[e] = acc[8 * i + e];
+        store_bf16_run<8>(orow + 64 * i, piece);
       }
     }
   }
@@ -1043,8 +1040,8 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     const bool whole = seg_t0 == 0 && hd.t == hd.tiles - 1;
     const int j = first_seg ? 0 : 1;
     first_seg = false;
-    {
-      const float sc0 = whole ? vsc / L0 : vsc, sc1 = whole ? vsc / L1 : vsc;
+    {  // normalised output (a partial slot holds acc / l too)
+      const float sc0 = vsc / L0, sc1 = vsc / L1;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         Oa[e] = (Oa[e] + Z0) * sc0;
@@ -1070,8 +1067,8 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
 
     // ---- part of a sequence: (m, l, acc) into this range's slot, then publish
     const size_t slot = ((static_cast<size_t>(k) * HG + hg) * 2 + j) * (hpc * G) + warp * G;
-    if (2 * c < G) store_f32_run<E>(a.ws_acc + (slot + 2 * c) * D + g * E, Oa);
-    if (2 * c + 1 < G) store_f32_run<E>(a.ws_acc + (slot + 2 * c + 1) * D + g * E, Ob);
+    if (2 * c < G) store_f16_run<E>(a.ws_acc + (slot + 2 * c) * D + g * E, Oa);
+    if (2 * c + 1 < G) store_f16_run<E>(a.ws_acc + (slot + 2 * c + 1) * D + g * E, Ob);
     if (g == 0) {
       if (2 * c < G) *reinterpret_cast<float2*>(a.ws_ml + 2 * (slot + 2 * c)) = make_float2(m0, L0);
       if (2 * c + 1 < G)

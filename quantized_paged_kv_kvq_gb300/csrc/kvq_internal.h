@@ -40,7 +40,7 @@ struct DecodeArgs {
   const int32_t* block_table;
   const int32_t* context_lens;
   const int8_t* signs;
-  float* ws_acc;  // [NC, head groups, 2, heads per group, D]: partial accumulators
+  __half* ws_acc;  // [NC, head groups, 2, heads per group, D]: partial outputs acc / l (fp16)
   float* ws_ml;   // [NC, head groups, 2, heads per group, 2]: partial (max, sum)
   unsigned long long* tags;    // [NC, head groups, 2]: the call's tag once a slot is written
   unsigned long long* claims;  // [S, head groups]: the call's tag once a merge is claimed
@@ -57,8 +57,6 @@ struct DecodeArgs {
   int max_blocks_per_seq;
   int max_context_len;
   int num_ctas;          // NC: stream-K ranges (CTAs per head group)
-  int split_h;           // ranges [0, split_h) weigh split_wa, the others split_wb
-  int split_wa, split_wb;
   float qk_scale;        // sm_scale * log2(e) [* k_scale for symmetric K]
   float v_scale;         // symmetric V: multiplies the output
   float cR;
