@@ -131,7 +131,7 @@ kvq_status kvq_write_cache(const kvq_cache_desc* cache, void* k_cache, void* v_c
  * needs for these sizes: partial results of sequences split between CTAs
  * (num_ctas * 2 * num_q_heads * (head_dim * 2 + 8) bytes: fp16 outputs and
  * fp32 (max, sum); 0 with one CTA)
- * two 8-byte completion tags per (CTA, group of 8 kv-heads) and one 8-byte
+ * six 8-byte tags and claims per (CTA, group of 8 kv-heads) and one 8-byte
  * merge claim per (sequence, group of 8 kv-heads).  Depends on the device's
  * SM count (current device).
  */

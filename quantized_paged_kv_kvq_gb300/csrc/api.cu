@@ -80,13 +80,14 @@ int auto_ctas(int num_seqs, int max_ctx, int head_groups, int sms) {
 
 // Workspace: per (range, head group, first/last segment of the range, head) a
 // partial output of D fp16 (acc / l) and its (max, sum) in f32; per (range,
-// head group, first/last segment) a 64-bit completion tag; per (sequence, head
-// group) a 64-bit merge claim.  One range needs none.
+// head group, first/last segment) three 64-bit words (completion tag, team
+// tag, team claim); per (sequence, head group) a 64-bit merge claim.  One
+// range needs none.
 size_t workspace_bytes_for(int num_seqs, int hq, int hkv, int d, int nc) {
   if (nc <= 1) return 0;
   const size_t rows = static_cast<size_t>(nc) * 2 * hq;
   const size_t groups = static_cast<size_t>(hkv / heads_per_cta(hkv));
-  return rows * (d * 2 + 2 * sizeof(float)) + static_cast<size_t>(nc) * groups * 2 * 8 +
+  return rows * (d * 2 + 2 * sizeof(float)) + static_cast<size_t>(nc) * groups * 2 * 8 * 3 +
          static_cast<size_t>(num_seqs) * groups * 8;
 }
 
@@ -239,8 +240,11 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
   a.ws_ml = need ? reinterpret_cast<float*>(static_cast<__half*>(workspace) + rows * cache->head_dim)
                  : nullptr;
   a.tags = need ? reinterpret_cast<unsigned long long*>(a.ws_ml + rows * 2) : nullptr;
-  a.claims = need ? a.tags + static_cast<size_t>(NC) * (cache->num_kv_heads / heads_per_cta(cache->num_kv_heads)) * 2
-                  : nullptr;
+  const size_t slot_words = static_cast<size_t>(NC) *
+                           (cache->num_kv_heads / heads_per_cta(cache->num_kv_heads)) * 2;
+  a.team_tags = need ? a.tags + slot_words : nullptr;
+  a.team_claims = need ? a.tags + 2 * slot_words : nullptr;
+  a.claims = need ? a.tags + 3 * slot_words : nullptr;
   a.epoch = next_epoch();
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;

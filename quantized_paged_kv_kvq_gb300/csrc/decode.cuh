@@ -531,6 +531,145 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long 
   }
 }
 
+constexpr int kTeam = 8;       // ranges merged together at the first level of a tree
+constexpr int kTreeRanges = 32;  // sequences over more ranges than this merge in two levels
+
+// Slot of range kk for the sequence whose tiles start at global tile ps: the
+// range's first segment (0) or its last (1).
+__device__ __forceinline__ long long slot_index(const DecodeArgs& a, long long T, long long ps,
+                                                int kk, int HG, int hg) {
+  return (static_cast<long long>(kk) * HG + hg) * 2 + (range_start(a, T, kk) >= ps ? 0 : 1);
+}
+
+// Log-sum-exp merge of slots, by the whole CTA (warp w merges its kv-head's G
+// query heads, four at a time).  The inputs are the slots of ranges r_first +
+// step*i (i < count) for the sequence starting at global tile ps, skipping a
+// range whose span of `step` ranges (clipped at r_last) holds no tile.  A slot
+// holds, per query head, the normalised output acc/l in fp16 and (m, l) in
+// fp32; the merge is out = sum_i 2^(m_i - M) l_i (acc_i/l_i) / sum_i 2^(m_i - M) l_i.
+// The result goes to the output rows of sequence s (dst < 0; with the inverse
+// rotation for KVarN) or, in the same slot format, to slot dst.  Lane (nn, r)
+// owns query head nn's dims 64i + 8r + e (i < DL/8, e < 8), so each 16-byte
+// load of a warp reads whole 128-byte lines; each lane reads every slot's
+// (m, l) itself, and the loads of PU slots are issued together.
+template <int D, bool KVARN>
+__device__ __forceinline__ void merge_slots(const DecodeArgs& a, int s, long long ps, long long T,
+                                            int HG, int hg, int warp, int lane, int hpc,
+                                            int r_first, int step, int count, int r_last,
+                                            long long dst) {
+  constexpr int LQ = 8;        // lanes per query head
+  constexpr int DL = D / LQ;   // dims per lane
+  constexpr int PU = 4;        // slots per batch of loads
+  const int G = a.gqa, rows = hpc * G;
+  const int r = lane % LQ;
+  const int h = hg * hpc + warp;
+#pragma unroll 1
+  for (int n0 = 0; n0 < G; n0 += 32 / LQ) {  // every lane runs every pass (shuffles below)
+    const int nn = n0 + lane / LQ;
+    const bool act = nn < G;
+    float M = -INFINITY, Lsum = 0.f;
+    float acc[DL];
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[e] = 0.f;
+#pragma unroll 1
+    for (int c0 = 0; c0 < count; c0 += 32) {  // slots c0 .. c0+31
+      // lane p: first slot row of input c0 + p, or -1 if its span holds no tile
+      long long base = -1;
+      if (c0 + lane < count) {
+        const int kk = r_first + step * (c0 + lane);
+        const long long r0 = range_start(a, T, kk);
+        const long long r1 = range_start(a, T, min(kk + step, r_last + 1));
+        if (r0 < r1) base = slot_index(a, T, ps, kk, HG, hg) * rows;
+      }
+      const int cn = min(32, count - c0);
+#pragma unroll 1
+      for (int p0 = 0; p0 < cn; p0 += PU) {
+        float ml[PU][2];
+        uint4 v[PU][DL / 8];
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+          const long long b = __shfl_sync(0xffffffffu, base, (p0 + u) & 31);
+          if (act && p0 + u < cn && b >= 0) {
+            const long long sl = b + warp * G + nn;
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + 2 * sl));
+            ml[u][0] = x.x;
+            ml[u][1] = x.y;
+            ldcg_halves<DL>(a.ws_acc + sl * D + 8 * r, v[u]);
+          } else {
+            ml[u][0] = -INFINITY;
+            ml[u][1] = 0.f;
+#pragma unroll
+            for (int i = 0; i < DL / 8; ++i) v[u][i] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        float bm = ml[0][0];
+#pragma unroll
+        for (int u = 1; u < PU; ++u) bm = fmaxf(bm, ml[u][0]);
+        if (bm > M) {  // raise the running maximum, rescaling what was summed so far
+          const float sc = fast_exp2(M - bm);
+          Lsum *= sc;
+#pragma unroll
+          for (int e = 0; e < DL; ++e) acc[e] *= sc;
+          M = bm;
+        }
+#pragma unroll
+        for (int u = 0; u < PU; ++u) {
+          const float w = fast_exp2(ml[u][0] - M) * ml[u][1];  // 2^(m - M) l
+          Lsum += w;
+#pragma unroll
+          for (int i = 0; i < DL / 8; ++i) {
+            const uint32_t q[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float2 f = half2_bits_to_float2(q[t]);
+              acc[8 * i + 2 * t] += w * f.x;
+              acc[8 * i + 2 * t + 1] += w * f.y;
+            }
+          }
+        }
+      }
+    }
+    const float il = act ? 1.0f / Lsum : 0.f;
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[e] *= il;
+    if (dst >= 0) {  // an intermediate result: back into slot format
+      if (act) {
+        const long long sl = dst * rows + warp * G + nn;
+#pragma unroll
+        for (int i = 0; i < DL / 8; ++i) {
+          float piece[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) piece[e] = acc[8 * i + e];
+          store_f16_run<8>(a.ws_acc + sl * D + 64 * i + 8 * r, piece);
+        }
+        if (r == 0) *reinterpret_cast<float2*>(a.ws_ml + 2 * sl) = make_float2(M, Lsum);
+      }
+      continue;
+    }
+    if constexpr (KVARN) {  // inverse rotation x = d . (cR * H y): the Walsh-Hadamard
+      // matrix is unchanged by a permutation of index bits, so the butterflies run
+      // over the local index (dim bits 0-2, 6) and then across the lanes (3-5)
+      fwht_lanes<DL, LQ>(acc, r);
+#pragma unroll
+      for (int e = 0; e < DL; ++e) {
+        const int dd = 64 * (e >> 3) + 8 * r + (e & 7);
+        const float sgn = (a.signs != nullptr && a.signs[dd] < 0) ? -1.f : 1.f;
+        acc[e] = __fmul_rn(acc[e], a.cR) * sgn;
+      }
+    }
+    if (act) {
+      uint16_t* orow = a.out + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G + nn) * D + 8 * r;
+#pragma unroll
+      for (int i = 0; i < DL / 8; ++i) {
+        float piece[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) piece[e] = acc[8 * i + e];
+        store_bf16_run<8>(orow + 64 * i, piece);
+      }
+    }
+  }
+}
+
 // Stream-K decode: CTA (k, hg) owns tiles [k*T/NC, (k+1)*T/NC) of the global
 // tile order (sequence-major, 16 tokens of all this group's heads per tile).
 // Thread 0 is also the producer that keeps the ring full.  A sequence the
@@ -1088,8 +1227,13 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     }
   }
 
-  // ---- merges: a partial segment is merged here once every other range of its
-  // sequence has published (a fence between this CTA's tag stores and its loads)
+  // ---- merges.  A CTA with a partial segment checks the tags of the sequence's
+  // other ranges (store-then-fence-then-load: at least one range sees them
+  // all) and the one that swaps the call's tag into the claim word merges.
+  // A sequence over more than kTreeRanges ranges merges in two levels instead:
+  // teams of kTeam consecutive ranges, each merged (by its member that wins the
+  // team's claim) into the slot of its first range, then the teams (by the team
+  // merger that sees every team's tag and wins the sequence's claim).
   __syncthreads();
   const long long Tm = scratch[0];
   if (warp == pub) {
@@ -1101,8 +1245,11 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
       const long long ps = scratch[12 + 2 * jj];
       const int tiles = static_cast<int>(info & 0xFFFFFFFFll);
       const int ka = range_of(a, ps, Tm), kb = range_of(a, ps + tiles - 1, Tm);
+      const bool tree = kb - ka + 1 > kTreeRanges;
+      const int lo = tree ? ka + (k - ka) / kTeam * kTeam : ka;
+      const int hi = tree ? min(kb, lo + kTeam - 1) : kb;
       bool done = true;
-      for (int kk = ka + lane; kk <= kb; kk += 32) {
+      for (int kk = lo + lane; kk <= hi; kk += 32) {
         const long long q0 = range_start(a, Tm, kk), q1 = range_start(a, Tm, kk + 1);
         if (kk == k || q0 >= q1) continue;  // this range, or an empty one
         const int j2 = (q0 >= ps) ? 0 : 1;
@@ -1110,9 +1257,11 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
           done = false;
       }
       done = __all_sync(0xffffffffu, done);
-      if (lane == 0) {  // one merge per sequence: the first to swap the tag into its claim word
-        if (!done || atomicExch(a.claims + static_cast<size_t>(info >> 32) * HG + hg, a.epoch) == a.epoch)
-          scratch[13 + 2 * jj] = -1;
+      if (lane == 0) {  // one merge per sequence (per team)
+        unsigned long long* claim =
+            tree ? a.team_claims + slot_index(a, Tm, ps, lo, HG, hg)
+                 : a.claims + static_cast<size_t>(info >> 32) * HG + hg;
+        if (!done || atomicExch(claim, a.epoch) == a.epoch) scratch[13 + 2 * jj] = -1;
       }
       __syncwarp();
     }
@@ -1123,8 +1272,45 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
   for (int pm = 0; pm < 2; ++pm) {
     const long long info = scratch[13 + 2 * pm];
     if (info < 0) continue;
-    merge_partials<D, KVARN>(a, static_cast<int>(info >> 32), scratch[12 + 2 * pm],
-                             static_cast<int>(info & 0xFFFFFFFFll), Tm, NC, HG, hg, warp, lane, hpc);
+    const int s = static_cast<int>(info >> 32), tiles = static_cast<int>(info & 0xFFFFFFFFll);
+    const long long ps = scratch[12 + 2 * pm];
+    const int ka = range_of(a, ps, Tm), kb = range_of(a, ps + tiles - 1, Tm);
+    if (kb - ka + 1 <= kTreeRanges) {
+      merge_partials<D, KVARN>(a, s, ps, tiles, Tm, NC, HG, hg, warp, lane, hpc);
+      continue;
+    }
+    const int nteams = (kb - ka) / kTeam + 1;
+    const int lo = ka + (k - ka) / kTeam * kTeam, hi = min(kb, lo + kTeam - 1);
+    const long long rep = slot_index(a, Tm, ps, lo, HG, hg);
+    merge_slots<D, KVARN>(a, s, ps, Tm, HG, hg, warp, lane, hpc, lo, 1, hi - lo + 1, kb, rep);
+    __syncthreads();  // every warp's rows of the team result are stored
+    if (warp == pub) {
+      if (lane == 0) {
+        __threadfence();
+        st_relaxed_u64(a.team_tags + rep, a.epoch);
+      }
+      __syncwarp();
+      __threadfence();
+      bool done = true;
+      for (int t = lane; t < nteams; t += 32) {
+        const int lo2 = ka + t * kTeam;
+        if (lo2 == lo) continue;
+        const long long q0 = range_start(a, Tm, lo2);
+        const long long q1 = range_start(a, Tm, min(lo2 + kTeam, kb + 1));
+        if (q0 >= q1) continue;  // a team of empty ranges
+        if (ld_relaxed_u64(a.team_tags + slot_index(a, Tm, ps, lo2, HG, hg)) != a.epoch)
+          done = false;
+      }
+      done = __all_sync(0xffffffffu, done);
+      if (lane == 0)  // one final merge per sequence
+        scratch[4 + pm] =
+            done && atomicExch(a.claims + static_cast<size_t>(s) * HG + hg, a.epoch) != a.epoch;
+      __syncwarp();
+      __threadfence();
+    }
+    __syncthreads();
+    if (scratch[4 + pm])
+      merge_slots<D, KVARN>(a, s, ps, Tm, HG, hg, warp, lane, hpc, ka, kTeam, nteams, kb, -1);
   }
 }
 

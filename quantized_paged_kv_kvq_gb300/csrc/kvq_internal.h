@@ -43,7 +43,9 @@ struct DecodeArgs {
   __half* ws_acc;  // [NC, head groups, 2, heads per group, D]: partial outputs acc / l (fp16)
   float* ws_ml;   // [NC, head groups, 2, heads per group, 2]: partial (max, sum)
   unsigned long long* tags;    // [NC, head groups, 2]: the call's tag once a slot is written
-  unsigned long long* claims;  // [S, head groups]: the call's tag once a merge is claimed
+  unsigned long long* team_tags;    // [NC, head groups, 2]: set once a team of ranges is merged
+  unsigned long long* team_claims;  // [NC, head groups, 2]: claim of a team's merge
+  unsigned long long* claims;       // [S, head groups]: claim of a sequence's final merge
   unsigned long long epoch;    // nonzero tag of this call
   int num_seqs;
   int num_q_heads;

@@ -109,10 +109,10 @@ def test_decode_validation(lib):
     n = ctypes.c_size_t(0)
     assert lib.kvq_decode_workspace_size_ex(ctypes.byref(d), 4, 32, 1024, 256,
                                             ctypes.byref(n)) == 0
-    # two partial slots per CTA and head, two completion tags per CTA and a merge
-    # claim per sequence (one head group)
+    # two partial slots per CTA and head; per slot a completion tag, a team tag
+    # and a team claim; a merge claim per sequence (one head group)
     # (fp16 partial outputs, fp32 (m, l))
-    assert n.value == 256 * 2 * 32 * (128 * 2 + 8) + 256 * 1 * 2 * 8 + 4 * 1 * 8
+    assert n.value == 256 * 2 * 32 * (128 * 2 + 8) + 256 * 1 * 2 * 8 * 3 + 4 * 1 * 8
     assert lib.kvq_decode_workspace_size_ex(ctypes.byref(d), 4, 32, 200, 1,
                                             ctypes.byref(n)) == 0
     assert n.value == 0  # one CTA: every sequence is whole, no workspace

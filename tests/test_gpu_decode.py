@@ -45,6 +45,20 @@ def test_split_invariance(name, ctas):
     assert_attention_close(got, ref, f"{name} ctas={ctas}")
 
 
+@pytest.mark.parametrize("name", ["llama8b_int8", "kvarn_131k"])
+@pytest.mark.parametrize("ctas", [33, 200])
+def test_long_sequence_merges_in_two_levels(name, ctas):
+    """One long sequence next to short ones, split over more than 32 ranges:
+    the split results are merged team by team, then across teams."""
+    lens = np.array([4000, 37, 1, 300], np.int32)
+    wl = W.workload(name, num_seqs=len(lens), context_lens=lens)
+    g = GpuRun(wl)
+    g.write()
+    got = out_numpy(g.decode(num_ctas=ctas))
+    assert_attention_close(got, OracleRun(wl).decode(), f"{name} ctas={ctas}")
+    assert kvq.kvq_get_device_error() == 0
+
+
 @pytest.mark.parametrize("name", ["llama8b_int8", "llama70b_int4", "kvarn_131k", "tiny_int8",
                                   "llama8b_e5m2"])
 def test_context_length_edge_cases(name):
