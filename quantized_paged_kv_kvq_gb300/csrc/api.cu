@@ -172,6 +172,7 @@ kvq_status kvq_write_cache(const kvq_cache_desc* cache, void* k_cache, void* v_c
   a.v_meta = static_cast<__half*>(cache->v_meta);
   a.num_kv_heads = cache->num_kv_heads;
   a.block_size = cache->block_size;
+  a.block_shift = cache->block_size == 16 ? 4 : 5;
   a.num_blocks = cache->num_blocks;
   // inv = 1/scale, one IEEE float32 division on the host
   volatile float one = 1.0f;

@@ -375,13 +375,20 @@ __device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int s) {
   return ctx <= 0 ? 0 : (min(ctx, a.max_context_len) + 15) >> 4;
 }
 
+// floor(n / d) for n >= 0, d > 0: a 32-bit division whenever both fit (the
+// 64-bit division is a long software sequence on this part)
+__device__ __forceinline__ long long div_floor(long long n, long long d) {
+  if (((static_cast<unsigned long long>(n) | static_cast<unsigned long long>(d)) >> 32) == 0)
+    return static_cast<unsigned>(n) / static_cast<unsigned>(d);
+  return n / d;
+}
 // First global tile of stream-K range k: ranges [k*T/NC, (k+1)*T/NC).
 __device__ __forceinline__ long long range_start(const DecodeArgs& a, long long T, int k) {
-  return T * k / a.num_ctas;
+  return div_floor(T * k, a.num_ctas);
 }
 // The range holding global tile x < T: the largest k with range_start(k) <= x.
 __device__ __forceinline__ int range_of(const DecodeArgs& a, long long x, long long T) {
-  return static_cast<int>(((x + 1) * a.num_ctas - 1) / T);
+  return static_cast<int>(div_floor((x + 1) * a.num_ctas - 1, T));
 }
 
 template <int N>

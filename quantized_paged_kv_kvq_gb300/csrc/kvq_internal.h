@@ -23,6 +23,7 @@ struct WriteArgs {
   __half* v_meta;
   int num_kv_heads;
   int block_size;
+  int block_shift;  // log2(block_size)
   int num_blocks;
   float k_inv;  // 1/k_scale (symmetric formats)
   float v_inv;

@@ -174,8 +174,8 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
     if (lane == 0) raise_error(1u);  // KVQ_DEVERR_SLOT_RANGE
     return;
   }
-  const int64_t blk = slot / a.block_size;
-  const int off = static_cast<int>(slot % a.block_size);
+  const int64_t blk = slot >> a.block_shift;
+  const int off = static_cast<int>(slot & (a.block_size - 1));
   const int sub = lane % LPR, grp = lane / LPR;
   const int Hkv = a.num_kv_heads;
 
@@ -392,8 +392,8 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
     if (lane == 0) raise_error(1u);  // KVQ_DEVERR_SLOT_RANGE
     return;
   }
-  const int64_t blk = slot / a.block_size;
-  const int off = static_cast<int>(slot % a.block_size);
+  const int64_t blk = slot >> a.block_shift;
+  const int off = static_cast<int>(slot & (a.block_size - 1));
   const int sub = lane % LPR, grp = lane / LPR;
   const int Hkv = a.num_kv_heads;
 
