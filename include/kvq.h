@@ -81,6 +81,12 @@ typedef enum {
  *   Dequantization: x = (code * scale + zero_point) [* sigma, then the
  *   inverse rotation].
  * Per-tensor scales (symmetric formats): x = code_value * k_scale (v_scale).
+ * Per-kv-head scales (symmetric formats, optional): k_head_scales /
+ *   v_head_scales, device fp32 [num_kv_heads], 4-byte aligned, each > 0; when
+ *   given, head h uses x = code_value * k_head_scales[h] (and codes
+ *   rne(x * (1 / k_head_scales[h]))) in place of k_scale.  The per-tensor
+ *   scales of the INT8 summary and PR #4893 made per attention head, as
+ *   PR #4893's thread leaves for later.  NULL: the per-tensor scale.
  * signs: device int8 [head_dim] of +1 / -1 (the rotation's diagonal), or
  *   NULL for all +1; read only with KVQ_FLAG_VARNORM_ROTATE.
  */
@@ -89,7 +95,7 @@ typedef struct {
   int32_t v_fmt;        /* kvq_format */
   int32_t num_kv_heads; /* >= 1 */
   int32_t head_dim;     /* 64 or 128 */
-  int32_t block_size;   /* 16 or 32 tokens per block */
+  int32_t block_size;   /* tokens per block: 16, 32, 64 or 128 */
   int32_t num_blocks;   /* >= 1 */
   uint32_t flags;       /* KVQ_FLAG_* */
   float k_scale;        /* symmetric K formats: > 0 (1.0 = uncalibrated fp8) */
@@ -97,6 +103,8 @@ typedef struct {
   void* k_meta;
   void* v_meta;
   const int8_t* signs;
+  const float* k_head_scales; /* NULL or device fp32 [num_kv_heads] (symmetric K) */
+  const float* v_head_scales; /* NULL or device fp32 [num_kv_heads] (symmetric V) */
 } kvq_cache_desc;
 
 /*
@@ -253,6 +261,19 @@ kvq_status kvq_hadamard(void* x, int32_t dtype, int64_t rows, int32_t head_dim,
  */
 kvq_status kvq_calibrate_scale(const void* x, int64_t n, float qmax, float* scale_out,
                                kvq_stream_t stream);
+
+/*
+ * kvq_calibrate_head_scales -- per-kv-head scales for the k_head_scales /
+ * v_head_scales of kvq_cache_desc: scales_out[h] = absmax over tokens t and
+ * dims d of x[t, h, d], divided by qmax in float32 (1.0 for an all-zero head).
+ * x: device bf16 [num_tokens, num_kv_heads, head_dim], row stride `stride`
+ * elements between tokens (>= num_kv_heads * head_dim, multiple of 8), 16-byte
+ * aligned, finite values; scales_out: device float [num_kv_heads], 4-byte
+ * aligned, overwritten.  head_dim: a multiple of 8.
+ */
+kvq_status kvq_calibrate_head_scales(const void* x, int64_t num_tokens, int32_t num_kv_heads,
+                                     int32_t head_dim, int64_t stride, float qmax,
+                                     float* scales_out, kvq_stream_t stream);
 
 /* Device error word bits. */
 #define KVQ_DEVERR_SLOT_RANGE 1u  /* a slot id past num_blocks*block_size */

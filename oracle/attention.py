@@ -50,12 +50,14 @@ def paged_decode(query, k_codes, k_meta, v_codes, v_meta, block_table, context_l
     out = np.zeros((s_count, hq, d))
     if pairs is None:
         pairs = [(s, h) for s in range(s_count) for h in range(hkv)]
+    # a scale may be one per kv-head (symmetric formats)
+    head = lambda sc, h: sc[h] if np.ndim(sc) == 1 else sc
     for s, h in pairs:
         ctx = int(context_lens[s])
         k = dequant_sequence(k_codes, k_meta, block_table[s], ctx, block_size, h, k_fmt,
-                             k_scale, kvarn, signs, d)
+                             head(k_scale, h), kvarn, signs, d)
         v = dequant_sequence(v_codes, v_meta, block_table[s], ctx, block_size, h, v_fmt,
-                             v_scale, kvarn, signs, d)
+                             head(v_scale, h), kvarn, signs, d)
         out[s, h * g:(h + 1) * g] = softmax_average(query[s, h * g:(h + 1) * g], k, v, sm_scale)
     return out
 

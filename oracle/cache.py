@@ -83,14 +83,22 @@ def alloc_cache(num_blocks, block_size, num_kv_heads, head_dim, fmt, kvarn, fill
 
 def write_cache(codes, meta, rows_thd: np.ndarray, slot_mapping, block_size, fmt, scale,
                 kvarn=False, signs=None):
-    """Quantize x [T, Hkv, D] and scatter into (codes, meta) in place."""
+    """Quantize x [T, Hkv, D] and scatter into (codes, meta) in place.
+
+    `scale` is one value for the tensor, or (symmetric formats) an array of
+    one value per kv-head, head h's rows quantized with scale[h]."""
     rows_thd = np.asarray(rows_thd, np.float32)
     t, hkv, d = rows_thd.shape
     slots = np.asarray(slot_mapping, np.int64)
     keep = slots >= 0
-    c, m = encode_rows(rows_thd.reshape(t * hkv, d), fmt, scale, kvarn, signs)
-    c = c.reshape(t, hkv, -1)[keep]
-    m = m.reshape(t, hkv, -1)[keep]
+    if np.ndim(scale) == 1:
+        parts = [encode_rows(rows_thd[:, h, :], fmt, scale[h], kvarn, signs) for h in range(hkv)]
+        c = np.stack([p[0] for p in parts], axis=1)[keep]
+        m = np.stack([p[1] for p in parts], axis=1)[keep]
+    else:
+        c, m = encode_rows(rows_thd.reshape(t * hkv, d), fmt, scale, kvarn, signs)
+        c = c.reshape(t, hkv, -1)[keep]
+        m = m.reshape(t, hkv, -1)[keep]
     blk = slots[keep] // block_size
     off = slots[keep] % block_size
     codes[blk, off] = c

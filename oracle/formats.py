@@ -155,6 +155,14 @@ def calibrate(x: np.ndarray, rule: str) -> np.float32:
     return F32(amax) / F32(qmax)
 
 
+def calibrate_heads(x_thd: np.ndarray, rule: str) -> np.ndarray:
+    """One scale per kv-head of x [T, Hkv, D]: calibrate() over each head's
+    values (the per-attention-head scales that PR #4893's thread leaves as a
+    later step)."""
+    x_thd = np.asarray(x_thd, np.float32)
+    return np.array([calibrate(x_thd[:, h, :], rule) for h in range(x_thd.shape[1])], np.float32)
+
+
 def inverse_scale(scale) -> np.float32:
     """inv = 1/scale, one IEEE float32 division, computed once per call."""
     return F32(1.0) / F32(scale)

@@ -35,7 +35,8 @@ kvq_status check_cache(const kvq_cache_desc* c) {
     return KVQ_ERR_INVALID_ARGUMENT;
   if (c->flags & ~KVQ_FLAG_VARNORM_ROTATE) return KVQ_ERR_INVALID_ARGUMENT;
   if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
-  if (c->block_size != 16 && c->block_size != 32) return KVQ_ERR_UNSUPPORTED;
+  if (c->block_size != 16 && c->block_size != 32 && c->block_size != 64 && c->block_size != 128)
+    return KVQ_ERR_UNSUPPORTED;  // a power of two >= 16: a 16-token tile never spans blocks
   const bool kvarn = (c->flags & KVQ_FLAG_VARNORM_ROTATE) != 0;
   if (!pairing_ok(c->k_fmt, c->v_fmt, kvarn)) return KVQ_ERR_UNSUPPORTED;
   if (!is_asym(c->k_fmt) && !(c->k_scale > 0.0f && isfinite(c->k_scale)))
@@ -47,6 +48,11 @@ kvq_status check_cache(const kvq_cache_desc* c) {
   if (is_asym(c->v_fmt) && (c->v_meta == nullptr || !aligned(c->v_meta, 16)))
     return KVQ_ERR_INVALID_ARGUMENT;
   if (kvarn && c->signs != nullptr && !aligned(c->signs, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+  // per-kv-head scales: symmetric formats only
+  if (c->k_head_scales != nullptr && (is_asym(c->k_fmt) || !aligned(c->k_head_scales, 4)))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->v_head_scales != nullptr && (is_asym(c->v_fmt) || !aligned(c->v_head_scales, 4)))
+    return KVQ_ERR_INVALID_ARGUMENT;
   return KVQ_OK;
 }
 
@@ -172,12 +178,14 @@ kvq_status kvq_write_cache(const kvq_cache_desc* cache, void* k_cache, void* v_c
   a.v_meta = static_cast<__half*>(cache->v_meta);
   a.num_kv_heads = cache->num_kv_heads;
   a.block_size = cache->block_size;
-  a.block_shift = cache->block_size == 16 ? 4 : 5;
+  a.block_shift = __builtin_ctz(static_cast<unsigned>(cache->block_size));
   a.num_blocks = cache->num_blocks;
   // inv = 1/scale, one IEEE float32 division on the host
   volatile float one = 1.0f;
   a.k_inv = is_asym(cache->k_fmt) ? 1.0f : one / cache->k_scale;
   a.v_inv = is_asym(cache->v_fmt) ? 1.0f : one / cache->v_scale;
+  a.k_head_scale = cache->k_head_scales;
+  a.v_head_scale = cache->v_head_scales;
   a.signs = cache->signs;
   a.cR = rotation_scale(cache->head_dim);
   const cudaError_t e =
@@ -253,13 +261,16 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
   a.gqa = num_q_heads / cache->num_kv_heads;
   a.heads_per_cta = heads_per_cta(cache->num_kv_heads);
   a.block_size = cache->block_size;
-  a.block_shift = cache->block_size == 16 ? 4 : 5;
+  a.block_shift = __builtin_ctz(static_cast<unsigned>(cache->block_size));
   a.num_blocks = cache->num_blocks;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.max_context_len = max_context_len;
   a.num_ctas = NC;
   a.qk_scale = sm_scale * kLog2e * (is_asym(cache->k_fmt) ? 1.0f : cache->k_scale);
   a.v_scale = is_asym(cache->v_fmt) ? 1.0f : cache->v_scale;
+  a.qk_base = sm_scale * kLog2e;
+  a.k_head_scale = cache->k_head_scales;
+  a.v_head_scale = cache->v_head_scales;
   a.cR = rotation_scale(cache->head_dim);
   cudaError_t e;
   const int kf = cache->k_fmt, vf = cache->v_fmt;
@@ -308,6 +319,23 @@ kvq_status kvq_calibrate_scale(const void* x, int64_t n, float qmax, float* scal
   if (sms <= 0) return KVQ_ERR_CUDA;
   const cudaError_t e =
       launch_calibrate(static_cast<const uint16_t*>(x), n, qmax, scale_out, stream, sms);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_calibrate_head_scales(const void* x, int64_t num_tokens, int32_t num_kv_heads,
+                                     int32_t head_dim, int64_t stride, float qmax,
+                                     float* scales_out, kvq_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 8 || head_dim % 8 ||
+      !(qmax > 0.0f && isfinite(qmax)) || scales_out == nullptr || !aligned(scales_out, 4))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (stride < static_cast<int64_t>(num_kv_heads) * head_dim || stride % 8)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_tokens > 0 && (x == nullptr || !aligned(x, 16))) return KVQ_ERR_INVALID_ARGUMENT;
+  const int sms = sm_count();
+  if (sms <= 0) return KVQ_ERR_CUDA;
+  const cudaError_t e =
+      launch_calibrate_heads(static_cast<const uint16_t*>(x), num_tokens, num_kv_heads, head_dim,
+                             stride, qmax, scales_out, stream, sms);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

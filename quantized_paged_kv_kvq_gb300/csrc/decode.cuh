@@ -922,7 +922,10 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
                                                   (g * C::VPS) / 16, (g * C::VPS) % 16);
   const uint32_t meta_k = m_off + warp * C::KMF * 32;
   const uint32_t meta_v = vm_off + warp * C::VMF * 32;
-  const float vsc = is_asym(VF) ? 1.0f : a.v_scale;
+  // this warp's kv-head scales (per-kv-head scales, when given, replace the tensor's)
+  const float vsc = is_asym(VF) ? 1.0f : (a.v_head_scale != nullptr ? a.v_head_scale[h] : a.v_scale);
+  const float qks = (!is_asym(KF) && a.k_head_scale != nullptr) ? a.qk_base * a.k_head_scale[h]
+                                                                : a.qk_scale;
 
   uint32_t qf[C::KSTEPS][2];
   float qsum0 = 0.f, qsum1 = 0.f;
@@ -1052,10 +1055,10 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
       for (int q = 0; q < 4; ++q) sacc[q] = sa[q] + sbb[q];
       if constexpr (!is_asym(KF)) {
         constexpr float bias = KF == INT8 ? 1152.0f : 0.0f;
-        sl[0] = (sacc[0] - bias * qsum0) * a.qk_scale;
-        sl[1] = (sacc[1] - bias * qsum1) * a.qk_scale;
-        sl[2] = (sacc[2] - bias * qsum0) * a.qk_scale;
-        sl[3] = (sacc[3] - bias * qsum1) * a.qk_scale;
+        sl[0] = (sacc[0] - bias * qsum0) * qks;
+        sl[1] = (sacc[1] - bias * qsum1) * qks;
+        sl[2] = (sacc[2] - bias * qsum0) * qks;
+        sl[3] = (sacc[3] - bias * qsum1) * qks;
       } else {
         sl[0] = (ks0 * (sacc[0] - 1024.0f * qsum0) + kz0 * qsum0) * a.qk_scale;
         sl[1] = (ks0 * (sacc[1] - 1024.0f * qsum1) + kz0 * qsum1) * a.qk_scale;

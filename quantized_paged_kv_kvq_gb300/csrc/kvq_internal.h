@@ -27,6 +27,8 @@ struct WriteArgs {
   int num_blocks;
   float k_inv;  // 1/k_scale (symmetric formats)
   float v_inv;
+  const float* k_head_scale;  // per-kv-head scales or nullptr (then k_inv / v_inv)
+  const float* v_head_scale;
   const int8_t* signs;
   float cR;  // float(1/sqrt(head_dim))
 };
@@ -62,6 +64,9 @@ struct DecodeArgs {
   int num_ctas;          // NC: stream-K ranges (CTAs per head group)
   float qk_scale;        // sm_scale * log2(e) [* k_scale for symmetric K]
   float v_scale;         // symmetric V: multiplies the output
+  float qk_base;         // sm_scale * log2(e)
+  const float* k_head_scale;  // per-kv-head scales or nullptr (then qk_scale / v_scale)
+  const float* v_head_scale;
   float cR;
 };
 
@@ -88,5 +93,8 @@ cudaError_t launch_hadamard(void* x, int dtype, int64_t rows, int head_dim, cons
 
 cudaError_t launch_calibrate(const uint16_t* x, int64_t n, float qmax, float* scale,
                              cudaStream_t st, int num_sms);
+cudaError_t launch_calibrate_heads(const uint16_t* x, int64_t num_tokens, int hkv, int d,
+                                   int64_t stride, float qmax, float* scales, cudaStream_t st,
+                                   int num_sms);
 
 }  // namespace kvq

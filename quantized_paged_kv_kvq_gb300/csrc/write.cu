@@ -210,11 +210,14 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
       const int h = hb + grp;
       const bool act = h < Hkv;
       float x[8];
+      // per-kv-head scales: 1/scale[h], correctly rounded like the host's division
+      const float kinv = a.k_head_scale != nullptr && act ? __frcp_rn(a.k_head_scale[h]) : a.k_inv;
+      const float vinv = a.v_head_scale != nullptr && act ? __frcp_rn(a.v_head_scale[h]) : a.v_inv;
       unpack8(rk[u], x);
-      quantize_store<D, KF, KVARN>(x, act, h, sub, row0 + h, a.k_cache, a.k_meta, a.k_inv, blk,
+      quantize_store<D, KF, KVARN>(x, act, h, sub, row0 + h, a.k_cache, a.k_meta, kinv, blk,
                                    off, Hkv, a.block_size, sign_bits, a.cR);
       unpack8(rv[u], x);
-      quantize_store<D, VF, KVARN>(x, act, h, sub, row0 + h, a.v_cache, a.v_meta, a.v_inv, blk,
+      quantize_store<D, VF, KVARN>(x, act, h, sub, row0 + h, a.v_cache, a.v_meta, vinv, blk,
                                    off, Hkv, a.block_size, sign_bits, a.cR);
     }
   }
@@ -478,6 +481,36 @@ __global__ void scale_from_absmax_kernel(float* scale, float qmax) {
   *scale = amax == 0.0f ? 1.0f : __fdiv_rn(amax, qmax);
 }
 
+// absmax per kv-head of x [T, Hkv, D] (row stride `stride`): one warp per
+// (token, head) row pass over 8-element pieces, atomicMax per head.
+__global__ void absmax_heads_kernel(const uint16_t* __restrict__ x, int64_t T, int hkv, int d,
+                                    int64_t stride, unsigned* out) {
+  const int pieces = d / 8;
+  const int64_t total = T * hkv * pieces;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += step) {
+    const int64_t row = i / pieces;
+    const int pc = static_cast<int>(i - row * pieces);
+    const int64_t t = row / hkv;
+    const int h = static_cast<int>(row - t * hkv);
+    const uint4 r = ldg_stream16(x + t * stride + static_cast<int64_t>(h) * d + pc * 8);
+    float v[8];
+    unpack8(r, v);
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
+    atomicMax(out + h, __float_as_uint(m));  // m >= 0: unsigned order is float order
+  }
+}
+
+__global__ void head_scales_from_absmax_kernel(float* scales, int hkv, float qmax) {
+  for (int h = threadIdx.x; h < hkv; h += blockDim.x) {
+    const float amax = __uint_as_float(reinterpret_cast<unsigned*>(scales)[h]);
+    scales[h] = amax == 0.0f ? 1.0f : __fdiv_rn(amax, qmax);
+  }
+}
+
 template <int D, int KF, int VF, bool KVARN>
 cudaError_t launch_write_t(const WriteArgs& a, cudaStream_t st) {
   const int64_t blocks = (a.num_tokens + kWriteWarps - 1) / kWriteWarps;
@@ -527,6 +560,24 @@ cudaError_t launch_write(const WriteArgs& a, int head_dim, int kf, int vf, bool 
   if (head_dim == 64) return dispatch_write_d<64>(a, kf, vf, kvarn, st);
   if (head_dim == 128) return dispatch_write_d<128>(a, kf, vf, kvarn, st);
   return cudaErrorNotSupported;
+}
+
+cudaError_t launch_calibrate_heads(const uint16_t* x, int64_t num_tokens, int hkv, int d,
+                                   int64_t stride, float qmax, float* scales, cudaStream_t st,
+                                   int num_sms) {
+  cudaError_t e = cudaMemsetAsync(scales, 0, sizeof(float) * hkv, st);
+  if (e != cudaSuccess) return e;
+  const int64_t total = num_tokens * hkv * (d / 8);
+  if (total > 0) {
+    const int64_t want = (total + 255) / 256;
+    const int blocks = static_cast<int>(want < 4LL * num_sms ? want : 4LL * num_sms);
+    absmax_heads_kernel<<<blocks, 256, 0, st>>>(x, num_tokens, hkv, d, stride,
+                                                 reinterpret_cast<unsigned*>(scales));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  head_scales_from_absmax_kernel<<<1, 256, 0, st>>>(scales, hkv, qmax);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_calibrate(const uint16_t* x, int64_t n, float qmax, float* scale,

@@ -41,7 +41,8 @@ class _CacheDesc(ctypes.Structure):
                 ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
                 ("flags", ctypes.c_uint32), ("k_scale", ctypes.c_float),
                 ("v_scale", ctypes.c_float), ("k_meta", ctypes.c_void_p),
-                ("v_meta", ctypes.c_void_p), ("signs", ctypes.c_void_p)]
+                ("v_meta", ctypes.c_void_p), ("signs", ctypes.c_void_p),
+                ("k_head_scales", ctypes.c_void_p), ("v_head_scales", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p
@@ -62,6 +63,7 @@ SIGNATURES = {
     "kvq_paged_decode_static_capacity": (_SZ, []),
     "kvq_hadamard": (_I32, [_P, _I32, _I64, _I32, _P, _I32, _P]),
     "kvq_calibrate_scale": (_I32, [_P, _I64, _F32, _P, _P]),
+    "kvq_calibrate_head_scales": (_I32, [_P, _I64, _I32, _I32, _I64, _F32, _P, _P]),
     "kvq_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "kvq_status_string": (ctypes.c_char_p, [_I32]),
     "kvq_version": (ctypes.c_char_p, []),
@@ -124,15 +126,17 @@ class KVCache:
     v_scale: float = 1.0
     varnorm_rotate: bool = False
     signs: Optional[torch.Tensor] = None
+    k_head_scales: Optional[torch.Tensor] = None  # fp32 [num_kv_heads] (symmetric K)
+    v_head_scales: Optional[torch.Tensor] = None  # fp32 [num_kv_heads] (symmetric V)
 
     def desc(self) -> _CacheDesc:
+        ptr = lambda t: None if t is None else t.data_ptr()
         return _CacheDesc(FMT[self.k_fmt], FMT[self.v_fmt], self.num_kv_heads, self.head_dim,
                           self.block_size, self.num_blocks,
                           FLAG_VARNORM_ROTATE if self.varnorm_rotate else 0,
-                          float(self.k_scale), float(self.v_scale),
-                          None if self.k_meta is None else self.k_meta.data_ptr(),
-                          None if self.v_meta is None else self.v_meta.data_ptr(),
-                          None if self.signs is None else self.signs.data_ptr())
+                          float(self.k_scale), float(self.v_scale), ptr(self.k_meta),
+                          ptr(self.v_meta), ptr(self.signs), ptr(self.k_head_scales),
+                          ptr(self.v_head_scales))
 
 
 def row_bytes(fmt: str, head_dim: int) -> int:
@@ -269,6 +273,17 @@ def kvq_calibrate_scale(x: torch.Tensor, qmax: float, out: torch.Tensor, stream=
     assert x.dtype == torch.bfloat16 and x.is_contiguous() and out.dtype == torch.float32
     st = lib.kvq_calibrate_scale(_ptr(x), x.numel(), float(qmax), _ptr(out), _stream(stream))
     _check(st, "kvq_calibrate_scale")
+    return out
+
+
+def kvq_calibrate_head_scales(x: torch.Tensor, qmax: float, out: torch.Tensor, stream=None):
+    """out (device float32 [Hkv]) <- per-kv-head absmax of x [T, Hkv, D] / qmax."""
+    lib = load_library()
+    assert x.dtype == torch.bfloat16 and x.dim() == 3 and out.dtype == torch.float32
+    assert x.stride(2) == 1 and x.stride(1) == x.shape[2] and out.numel() == x.shape[1]
+    st = lib.kvq_calibrate_head_scales(_ptr(x), x.shape[0], x.shape[1], x.shape[2], x.stride(0),
+                                       float(qmax), _ptr(out), _stream(stream))
+    _check(st, "kvq_calibrate_head_scales")
     return out
 
 

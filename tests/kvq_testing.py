@@ -39,7 +39,7 @@ def oracle_scale(x: np.ndarray, rule) -> np.float32:
 class GpuRun:
     """Device tensors of a workload plus the library's cache after the write."""
 
-    def __init__(self, wl: W.Workload, fill: int = 0xAA, device="cuda"):
+    def __init__(self, wl: W.Workload, fill: int = 0xAA, device="cuda", head_scales=False):
         self.wl = wl
         self.key = bf16(wl.key, device)
         self.value = bf16(wl.value, device)
@@ -54,6 +54,14 @@ class GpuRun:
         self.cache = kvq.alloc_kv_cache(wl.k_fmt, wl.v_fmt, wl.num_blocks, wl.block_size,
                                         wl.num_kv_heads, wl.head_dim, self.k_scale, self.v_scale,
                                         wl.kvarn, self.signs, device=device, fill=fill)
+        if head_scales:  # per-kv-head scales, calibrated on the GPU
+            qmax = {"absmax/127": 127.0, "absmax/448": 448.0}
+            for x, rule, attr in ((self.key, wl.k_scale_rule, "k_head_scales"),
+                                  (self.value, wl.v_scale_rule, "v_head_scales")):
+                if rule in qmax:
+                    hs = torch.empty(wl.num_kv_heads, dtype=torch.float32, device=device)
+                    kvq.kvq_calibrate_head_scales(x, qmax[rule], hs)
+                    setattr(self.cache, attr, hs)
 
     def write(self):
         kvq.kvq_write_cache(self.cache, self.key, self.value, self.slots)
@@ -80,10 +88,15 @@ class GpuRun:
 class OracleRun:
     """The oracle's own cache for (a subset of the tokens of) a workload."""
 
-    def __init__(self, wl: W.Workload, seqs=None, fill: int = 0xAA):
+    def __init__(self, wl: W.Workload, seqs=None, fill: int = 0xAA, head_scales=False):
         self.wl = wl
         self.k_scale = oracle_scale(wl.key, wl.k_scale_rule)
         self.v_scale = oracle_scale(wl.value, wl.v_scale_rule)
+        if head_scales:  # per-kv-head scales where the format is calibrated
+            if wl.k_scale_rule not in (None, "1.0"):
+                self.k_scale = OF.calibrate_heads(wl.key, wl.k_scale_rule)
+            if wl.v_scale_rule not in (None, "1.0"):
+                self.v_scale = OF.calibrate_heads(wl.value, wl.v_scale_rule)
         kc, km = OC.alloc_cache(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim,
                                 wl.k_fmt, wl.kvarn, fill)
         vc, vm = OC.alloc_cache(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim,

@@ -93,6 +93,17 @@ def _decode(lib, desc, **kw):
                                    a["ws"], a["wsb"], None)
 
 
+def test_head_scales_validation(lib):
+    # per-kv-head scales belong to symmetric formats only
+    assert _decode(lib, _desc(k_fmt=4, v_fmt=4, k_meta=FAKE, v_meta=FAKE,
+                              k_head_scales=FAKE)) == 1
+    assert _decode(lib, _desc(v_head_scales=FAKE + 2)) == 1  # misaligned
+    st = lib.kvq_calibrate_head_scales(FAKE, 10, 8, 128, 8 * 128 - 8, 127.0, FAKE, None)
+    assert st == 1  # token stride shorter than a token
+    assert lib.kvq_calibrate_head_scales(FAKE, 10, 8, 60, 480, 127.0, FAKE, None) == 1  # D % 8
+    assert lib.kvq_calibrate_head_scales(FAKE, 10, 8, 128, 1024, 0.0, FAKE, None) == 1
+
+
 def test_decode_validation(lib):
     d = _desc()
     assert _decode(lib, d, hq=30) == 1  # not a multiple of the kv heads

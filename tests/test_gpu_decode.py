@@ -91,16 +91,27 @@ def test_block_permutation_gives_identical_output():
     assert torch.equal(out1, out2)
 
 
-def test_block_size_16_and_32_agree():
-    lens = np.array([33, 100, 257, 5], np.int32)
+@pytest.mark.parametrize("name", ["llama8b_int8", "kvarn_131k"])
+def test_block_sizes_agree(name):
+    """Pages of 16, 32, 64 and 128 tokens: codes bit-exact with the oracle's
+    cache of the same page size, outputs within tolerance and alike."""
+    lens = np.array([33, 100, 257, 5, 300], np.int32)
     outs = []
-    for bs in (16, 32):
-        wl = W.workload("llama8b_int8", num_seqs=4, context_lens=lens, block_size=bs)
+    for bs in (16, 32, 64, 128):
+        wl = W.workload(name, num_seqs=len(lens), context_lens=lens, block_size=bs)
         g = GpuRun(wl)
         g.write()
-        outs.append(out_numpy(g.decode()))
-        assert_attention_close(outs[-1], OracleRun(wl).decode(), f"bs={bs}")
-    assert_attention_close(outs[0], outs[1], "bs16 vs bs32")
+        o = OracleRun(wl)
+        kc, km, vc, vm = g.cache_numpy()
+        assert np.array_equal(kc, o.kc) and np.array_equal(vc, o.vc), f"bs={bs}: codes differ"
+        if km is not None:
+            assert np.array_equal(km, o.km) and np.array_equal(vm, o.vm), f"bs={bs}: meta differs"
+        for ctas in (0, 7):
+            outs.append(out_numpy(g.decode(num_ctas=ctas)))
+            assert_attention_close(outs[-1], o.decode(), f"{name} bs={bs} ctas={ctas}")
+    for other in outs[1:]:
+        assert_attention_close(outs[0], other, f"{name}: page sizes")
+    assert kvq.kvq_get_device_error() == 0
 
 
 def test_bad_block_id_is_flagged_not_faulted():
@@ -145,4 +156,17 @@ def test_decode_full_size_sampled(name):
     sel_ref = np.stack([ref[s, q] for s, q in rows])
     assert_attention_close(sel_got, sel_ref, name)
     assert np.all(np.isfinite(got))
+    assert kvq.kvq_get_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["llama8b_int8", "llama8b_e4m3k_int8v"])
+@pytest.mark.parametrize("ctas", [1, 7, 0])
+def test_per_head_scales_decode(name, ctas):
+    """Decode with per-kv-head scales matches the oracle with the same scales
+    (and differs from the per-tensor result, so the scales are used)."""
+    wl = W.workload(name, num_seqs=4, ctx_lo=50, ctx_hi=700)
+    g = GpuRun(wl, head_scales=True)
+    g.write()
+    got = out_numpy(g.decode(num_ctas=ctas))
+    assert_attention_close(got, OracleRun(wl, head_scales=True).decode(), f"{name} ctas={ctas}")
     assert kvq.kvq_get_device_error() == 0

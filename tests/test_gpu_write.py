@@ -157,3 +157,19 @@ def test_write_full_size_sampled(name):
         vm = g.cache.v_meta[blks].view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.array_equal(km, o.km[bl]) and np.array_equal(vm, o.vm[bl])
     assert kvq.kvq_get_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["llama8b_int8", "llama8b_e4m3k_int8v", "tiny_int8"])
+def test_per_head_scales_calibration_and_codes_bit_exact(name):
+    """Per-kv-head scales: the GPU calibration equals the oracle's per head, and
+    the codes written with them equal the oracle's."""
+    wl = W.workload(name, num_seqs=3, ctx_lo=20, ctx_hi=300)
+    g = GpuRun(wl, head_scales=True)
+    o = OracleRun(wl, head_scales=True)
+    for attr, ref in (("k_head_scales", o.k_scale), ("v_head_scales", o.v_scale)):
+        got = getattr(g.cache, attr)
+        assert got is not None and np.array_equal(got.cpu().numpy(), np.asarray(ref, np.float32))
+    g.write()
+    kc, _, vc, _ = g.cache_numpy()
+    assert np.array_equal(kc, o.kc) and np.array_equal(vc, o.vc)
+    assert kvq.kvq_get_device_error() == 0
