@@ -71,7 +71,9 @@ class GpuRun:
         sm = float(OA.default_sm_scale(wl.head_dim)) if sm_scale is None else sm_scale
         nbytes = kvq.kvq_decode_workspace_size(self.cache, wl.num_seqs, wl.num_q_heads,
                                                wl.max_context_len, num_ctas)
+        # arbitrary bytes: the counters inside must not depend on the contents
         ws = torch.empty(max(nbytes, 16) // 4 + 4, dtype=torch.float32, device=self.query.device)
+        ws.view(torch.int32).random_()
         if out is None:
             out = torch.empty_like(self.query)
         kvq.kvq_paged_decode(self.cache, self.query, out, self.block_table, self.context_lens,
