@@ -33,9 +33,10 @@ sys.path.insert(0, ROOT)
 DEFAULT_WORKLOAD = "llama8b_int8"
 METRIC = "quantized paged decode: effective KV GB/s vs HBM peak; decode & cache-write tok/s"
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SOURCES = ["decode.cuh", "decode_launch.cuh", "kvq_device.cuh", "decode_d128_sym.cu",
-                  "decode_d128_asym.cu", "decode_d64_sym.cu", "decode_d64_asym.cu"]
-WRITE_SOURCES = ["write.cu", "kvq_device.cuh"]
+DECODE_SOURCES = ["decode.cuh", "decode_launch.cuh", "kvq_device.cuh", "quant_row.cuh",
+                  "decode_d128_sym.cu", "decode_d128_asym.cu", "decode_d64_sym.cu",
+                  "decode_d64_asym.cu"]
+WRITE_SOURCES = ["write.cu", "kvq_device.cuh", "quant_row.cuh"]
 
 
 def parse_args(argv=None):
@@ -49,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-append", action="store_true",
+                   help="skip the fused append-and-decode step timing")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
     return p.parse_args(argv)
@@ -441,6 +444,47 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
                 "traffic": profiled_traffic(args.workload, "write_cache"),
                 "algorithmic_bytes": wbytes}
 
+    # one decode step that brings its own token (one per sequence): the fused
+    # append-and-decode launch against a cache write of those tokens followed by
+    # the decode (both with a flushed L2; outside the timed region above)
+    step_lat = None
+    if not args.no_append:
+        last = np.cumsum(wl.context_lens.astype(np.int64)) - 1
+        has = wl.context_lens > 0
+        rows = torch.from_numpy(np.where(has, last, 0)).to(dev)
+        new_k, new_v = key[rows].contiguous(), value[rows].contiguous()
+        last_slots = torch.from_numpy(np.where(has, wl.slot_mapping[np.where(has, last, 0)],
+                                               -1)).to(dev)
+        n_app = max(3, min(K, 200))
+
+        def fused(ev):
+            flush_l2()
+            ev[0].record()
+            kvq.kvq_decode_append(cache, new_k, new_v, query, out, block_table, ctx_lens,
+                                  wl.max_context_len, sm_scale, ws, P)
+            ev[1].record()
+
+        def unfused(ev):
+            flush_l2()
+            ev[0].record()
+            kvq.kvq_write_cache(cache, new_k, new_v, last_slots)
+            kvq.kvq_paged_decode(*dargs)
+            ev[1].record()
+
+        res = {}
+        for name, fn in (("fused", fused), ("unfused", unfused)):
+            for _ in range(3):
+                fn(mk())
+            evs = [mk() for _ in range(n_app)]
+            for ev in evs:
+                fn(ev)
+            torch.cuda.synchronize()
+            ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
+            res[name] = max_over_ranks([float(np.median(ms)) * 1e3], dev)[0]
+        step_lat = {"fused_append_decode_us": res["fused"],
+                    "write_then_decode_us": res["unfused"], "steps": n_app,
+                    "stat": "median, L2 flushed before each step", "tokens_per_step": int(has.sum())}
+
     # end to end through the public API: pinned host inputs in, result out
     e2e = None
     if not args.no_e2e:
@@ -508,6 +552,7 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
         "roofline_write": rl_write,
         "decode_frac_of_hbm": gbs / world / hbm,
         "e2e": e2e,
+        "decode_step_append": step_lat,
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,

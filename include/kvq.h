@@ -202,6 +202,42 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
                                size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * kvq_decode_append -- one decode step with the step's own key and value:
+ * the new token of every sequence is quantized into the paged cache and the
+ * query attends to the context including it, in one kernel launch (the
+ * "write_to_paged_cache" store and the paged-attention read of issue #4025
+ * 'Support for 4-bit KV Cache in paged-attention op', section 'methods',
+ * items 2-3, for the decoding phase).
+ *
+ * new_key, new_value: device bf16 [num_seqs, num_kv_heads, head_dim]; heads
+ *   and elements contiguous, consecutive sequences `key_stride` /
+ *   `value_stride` elements apart (>= num_kv_heads*head_dim, multiple of 8);
+ *   16-byte aligned.
+ * context_lens counts the new token: for a sequence with context_len n > 0,
+ *   row s is written at position n-1, i.e. at block block_table[s][(n-1) /
+ *   block_size], offset (n-1) % block_size, and the attention runs over all
+ *   n positions.  A sequence with n = 0 writes nothing (out = 0).  A block id
+ *   outside [0, num_blocks) sets KVQ_DEVERR_BLOCK_RANGE and writes nothing.
+ * Codes and metadata: exactly those kvq_write_cache stores for the same rows
+ *   and slots (same formats, scales, per-head scales and KVarN transform).
+ * Output: that of kvq_paged_decode_ex on the cache after the write.
+ * The token at position n-1 must be written by this call alone: another call
+ *   (or kernel) that writes the same slots or reads them while this one runs
+ *   races with it.
+ * The caches are written, so k_cache / v_cache (and the metadata in `cache`)
+ *   must be writable.  Other arguments, the workspace and its size are those
+ *   of kvq_paged_decode_ex (num_ctas included).
+ */
+kvq_status kvq_decode_append(const kvq_cache_desc* cache, void* k_cache, void* v_cache,
+                             const void* new_key, const void* new_value, int64_t key_stride,
+                             int64_t value_stride, void* out, const void* query,
+                             int32_t num_seqs, int32_t num_q_heads,
+                             const int32_t* block_table, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t max_context_len,
+                             float sm_scale, int32_t num_ctas, void* workspace,
+                             size_t workspace_bytes, kvq_stream_t stream);
+
+/*
  * kvq_paged_decode_static -- kvq_paged_decode_ex for callers that cannot
  * allocate device memory.  None of the source pages has a counterpart of
  * this entry point: it exists for integration, not for the method.

@@ -211,12 +211,24 @@ kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_se
   return kvq_decode_workspace_size_ex(cache, num_seqs, num_q_heads, max_context_len, 0, bytes);
 }
 
-kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
-                               const void* v_cache, void* out, const void* query,
-                               int32_t num_seqs, int32_t num_q_heads, const int32_t* block_table,
-                               int32_t max_blocks_per_seq, const int32_t* context_lens,
-                               int32_t max_context_len, float sm_scale, int32_t num_ctas,
-                               void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The new-token rows of kvq_decode_append (nullptr key: a plain decode).
+struct AppendRows {
+  const void* key = nullptr;
+  const void* value = nullptr;
+  int64_t key_stride = 0;
+  int64_t value_stride = 0;
+};
+
+kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const void* v_cache,
+                       void* out, const void* query, int32_t num_seqs, int32_t num_q_heads,
+                       const int32_t* block_table, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t max_context_len, float sm_scale,
+                       int32_t num_ctas, void* workspace, size_t workspace_bytes,
+                       const AppendRows& app, kvq_stream_t stream) {
   int NC = 0;
   kvq_status st = decode_shape(cache, num_seqs, num_q_heads, max_context_len, num_ctas, &NC);
   if (st != KVQ_OK) return st;
@@ -272,6 +284,18 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
   a.k_head_scale = cache->k_head_scales;
   a.v_head_scale = cache->v_head_scales;
   a.cR = rotation_scale(cache->head_dim);
+  a.new_key = static_cast<const uint16_t*>(app.key);
+  a.new_value = static_cast<const uint16_t*>(app.value);
+  a.new_key_stride = app.key_stride;
+  a.new_value_stride = app.value_stride;
+  const bool append = app.key != nullptr;
+  a.k_cache_w = append ? static_cast<uint8_t*>(const_cast<void*>(k_cache)) : nullptr;
+  a.v_cache_w = append ? static_cast<uint8_t*>(const_cast<void*>(v_cache)) : nullptr;
+  a.k_meta_w = append ? static_cast<__half*>(cache->k_meta) : nullptr;
+  a.v_meta_w = append ? static_cast<__half*>(cache->v_meta) : nullptr;
+  volatile float one = 1.0f;  // 1/scale, one IEEE float32 division, as kvq_write_cache
+  a.k_inv = is_asym(cache->k_fmt) ? 1.0f : one / cache->k_scale;
+  a.v_inv = is_asym(cache->v_fmt) ? 1.0f : one / cache->v_scale;
   cudaError_t e;
   const int kf = cache->k_fmt, vf = cache->v_fmt;
   if (is_asym(kf)) {
@@ -283,6 +307,50 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
   }
   if (e == cudaErrorNotSupported) return KVQ_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
+                               const void* v_cache, void* out, const void* query,
+                               int32_t num_seqs, int32_t num_q_heads, const int32_t* block_table,
+                               int32_t max_blocks_per_seq, const int32_t* context_lens,
+                               int32_t max_context_len, float sm_scale, int32_t num_ctas,
+                               void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+  return decode_call(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
+                     max_blocks_per_seq, context_lens, max_context_len, sm_scale, num_ctas,
+                     workspace, workspace_bytes, AppendRows{}, stream);
+}
+
+kvq_status kvq_decode_append(const kvq_cache_desc* cache, void* k_cache, void* v_cache,
+                             const void* new_key, const void* new_value, int64_t key_stride,
+                             int64_t value_stride, void* out, const void* query,
+                             int32_t num_seqs, int32_t num_q_heads, const int32_t* block_table,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens,
+                             int32_t max_context_len, float sm_scale, int32_t num_ctas,
+                             void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (num_seqs > 0) {
+    if (!new_key || !new_value || !aligned(new_key, 16) || !aligned(new_value, 16))
+      return KVQ_ERR_INVALID_ARGUMENT;
+    const int64_t row = static_cast<int64_t>(cache->num_kv_heads) * cache->head_dim;
+    if (key_stride < row || value_stride < row || key_stride % 8 || value_stride % 8)
+      return KVQ_ERR_INVALID_ARGUMENT;
+    if (!write_supported(cache->k_fmt, cache->v_fmt,
+                         (cache->flags & KVQ_FLAG_VARNORM_ROTATE) != 0))
+      return KVQ_ERR_UNSUPPORTED;
+  }
+  AppendRows app;
+  app.key = new_key;
+  app.value = new_value;
+  app.key_stride = key_stride;
+  app.value_stride = value_stride;
+  return decode_call(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
+                     max_blocks_per_seq, context_lens, max_context_len, sm_scale, num_ctas,
+                     workspace, workspace_bytes, app, stream);
 }
 
 kvq_status kvq_paged_decode(const kvq_cache_desc* cache, const void* k_cache,

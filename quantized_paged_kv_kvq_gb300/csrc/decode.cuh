@@ -37,6 +37,7 @@
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "quant_row.cuh"
 
 namespace kvq {
 
@@ -677,6 +678,73 @@ __device__ __forceinline__ void merge_slots(const DecodeArgs& a, int s, long lon
   }
 }
 
+// New-token append, run by every warp of a CTA before its first tile load:
+// the token at position ctx-1 of each sequence whose last tile lies in
+// [R0, R1) is quantized into the caches, this warp's kv-head h only, with the
+// row code of the cache write (so the codes equal kvq_write_cache's for the
+// slot block_table[s][(ctx-1) / bs] * bs + (ctx-1) % bs).  That tile belongs
+// to this range alone, so no other CTA reads the new row.  The warps walk the
+// sequences from the range's first one, 32 at a time (a lane per sequence,
+// prefix sum of tile counts, ballot of those that end inside the range).
+template <int D, int KF, int VF, bool KVARN>
+__device__ __forceinline__ void append_new_tokens(const DecodeArgs& a, long long R0, long long R1,
+                                               int s0, long long ps0, int h, int lane) {
+  constexpr int LPR = RowGeom<D>::LPR;
+  const int sub = lane % LPR;
+  uint32_t sign_bits = 0;
+  if constexpr (KVARN) {
+    if (a.signs != nullptr) {
+      const uint2 sg = *reinterpret_cast<const uint2*>(a.signs + sub * 8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t byte = ((i < 4 ? sg.x : sg.y) >> (8 * (i & 3))) & 0xFFu;
+        sign_bits |= (byte & 0x80u) ? (1u << i) : 0u;
+      }
+    }
+  }
+  const float kinv = (!is_asym(KF) && a.k_head_scale != nullptr) ? __frcp_rn(a.k_head_scale[h]) : a.k_inv;
+  const float vinv = (!is_asym(VF) && a.v_head_scale != nullptr) ? __frcp_rn(a.v_head_scale[h]) : a.v_inv;
+  const int S = a.num_seqs, Hkv = a.num_kv_heads;
+  long long ps = ps0;  // first tile of sequence `base`
+  for (int base = s0; base < S && ps < R1; base += 32) {
+    const int s = base + lane;
+    const int cx = s < S ? a.context_lens[s] : 0;
+    const int cc = cx <= 0 ? 0 : min(cx, a.max_context_len);
+    const long long v = (cc + 15) >> 4;
+    long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long last = ps + incl - 1;  // last tile of sequence s
+    unsigned mine = __ballot_sync(0xffffffffu, v > 0 && last >= R0 && last < R1);
+    while (mine != 0u) {
+      const int src = __ffs(mine) - 1;
+      mine &= mine - 1u;
+      const int sq = base + src;
+      const int pos = __shfl_sync(0xffffffffu, cc, src) - 1;
+      const int blk = a.block_table[static_cast<size_t>(sq) * a.max_blocks_per_seq + (pos >> a.block_shift)];
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (lane == 0) raise_error(2u);  // KVQ_DEVERR_BLOCK_RANGE: nothing written
+        continue;
+      }
+      const int off = pos & (a.block_size - 1);
+      const size_t row = (static_cast<size_t>(blk) * a.block_size + off) * Hkv + h;
+      float x[8];
+      unpack8(*reinterpret_cast<const uint4*>(a.new_key + static_cast<size_t>(sq) * a.new_key_stride +
+                                              static_cast<size_t>(h) * D + sub * 8), x);
+      quantize_store<D, KF, KVARN>(x, lane < LPR, h, sub, row, a.k_cache_w, a.k_meta_w, kinv, blk,
+                                   off, Hkv, a.block_size, sign_bits, a.cR);
+      unpack8(*reinterpret_cast<const uint4*>(a.new_value + static_cast<size_t>(sq) * a.new_value_stride +
+                                              static_cast<size_t>(h) * D + sub * 8), x);
+      quantize_store<D, VF, KVARN>(x, lane < LPR, h, sub, row, a.v_cache_w, a.v_meta_w, vinv, blk,
+                                   off, Hkv, a.block_size, sign_bits, a.cR);
+    }
+    ps += __shfl_sync(0xffffffffu, incl, 31);
+  }
+}
+
 // Stream-K decode: CTA (k, hg) owns tiles [k*T/NC, (k+1)*T/NC) of the global
 // tile order (sequence-major, 16 tokens of all this group's heads per tile).
 // Thread 0 is also the producer that keeps the ring full.  A sequence the
@@ -805,6 +873,12 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
   const int s_first = static_cast<int>(scratch[1]);
   const long long ps_first = scratch[2];
   prefetch_q(s_first);
+  if (a.new_key != nullptr) {  // new-token append: codes stored before any tile is loaded
+    append_new_tokens<D, KF, VF, KVARN>(a, R0, R1, s_first, ps_first, h, lane);
+    // the stores (generic proxy) before the tensor loads (async proxy) the
+    // barrier below lets thread 0 issue
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
 
   if (threadIdx.x == 0) {
     scratch[0] = T;

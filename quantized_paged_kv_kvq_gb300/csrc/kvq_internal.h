@@ -68,6 +68,19 @@ struct DecodeArgs {
   const float* k_head_scale;  // per-kv-head scales or nullptr (then qk_scale / v_scale)
   const float* v_head_scale;
   float cR;
+  // New-token append (kvq_decode_append); new_key == nullptr for a plain decode.
+  // The token at position context_lens[s] - 1 of sequence s comes from row s
+  // of new_key / new_value (bf16 [S, Hkv, D], row strides in elements).
+  const uint16_t* new_key;
+  const uint16_t* new_value;
+  int64_t new_key_stride;
+  int64_t new_value_stride;
+  uint8_t* k_cache_w;  // the same caches, writable
+  uint8_t* v_cache_w;
+  __half* k_meta_w;
+  __half* v_meta_w;
+  float k_inv;  // 1/k_scale (symmetric formats, per-tensor scales)
+  float v_inv;
 };
 
 cudaError_t launch_write(const WriteArgs& a, int head_dim, int kf, int vf, bool kvarn,

@@ -58,6 +58,8 @@ SIGNATURES = {
                                 _SZ, _P]),
     "kvq_paged_decode_ex": (_I32, [_DESC, _P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _I32, _F32,
                                    _I32, _P, _SZ, _P]),
+    "kvq_decode_append": (_I32, [_DESC, _P, _P, _P, _P, _I64, _I64, _P, _P, _I32, _I32, _P, _I32,
+                                 _P, _I32, _F32, _I32, _P, _SZ, _P]),
     "kvq_paged_decode_static": (_I32, [_DESC, _P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _I32,
                                        _F32, _I32, _P]),
     "kvq_paged_decode_static_capacity": (_SZ, []),
@@ -226,6 +228,33 @@ def kvq_paged_decode(cache: KVCache, query: torch.Tensor, out: torch.Tensor,
     """out[s, h] = softmax(sm_scale q k^T) v over the paged cache (bf16 [S, Hq, D])."""
     return _decode_call("kvq_paged_decode_ex", cache, query, out, block_table, context_lens,
                         max_context_len, sm_scale, workspace, num_ctas, stream)
+
+
+def kvq_decode_append(cache: KVCache, new_key: torch.Tensor, new_value: torch.Tensor,
+                      query: torch.Tensor, out: torch.Tensor, block_table: torch.Tensor,
+                      context_lens: torch.Tensor, max_context_len: int, sm_scale: float,
+                      workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                      stream=None) -> torch.Tensor:
+    """One decode step in one launch: row s of new_key / new_value (bf16 [S, Hkv, D],
+    sequence stride free) is quantized into the cache at position context_lens[s] - 1,
+    then out = the paged decode over the context including it."""
+    lib = load_library()
+    assert new_key.dtype == torch.bfloat16 and new_value.dtype == torch.bfloat16
+    assert query.dtype == torch.bfloat16 and out.dtype == torch.bfloat16
+    assert query.is_contiguous() and out.is_contiguous()
+    assert block_table.dtype == torch.int32 and context_lens.dtype == torch.int32
+    assert block_table.is_contiguous()
+    s, hq, _ = query.shape
+    d = cache.desc()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kvq_decode_append(ctypes.byref(d), _ptr(cache.k_cache), _ptr(cache.v_cache),
+                               _ptr(new_key), _ptr(new_value), new_key.stride(0),
+                               new_value.stride(0), _ptr(out), _ptr(query), s, hq,
+                               _ptr(block_table), block_table.shape[1], _ptr(context_lens),
+                               max_context_len, float(sm_scale), num_ctas, _ptr(workspace),
+                               ws_bytes, _stream(stream))
+    _check(st, "kvq_decode_append")
+    return out
 
 
 def kvq_paged_decode_static(cache: KVCache, query: torch.Tensor, out: torch.Tensor,

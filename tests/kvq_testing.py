@@ -124,6 +124,41 @@ class OracleRun:
                                self.v_scale, sm, wl.kvarn, wl.signs, pairs=pairs)
 
 
+def random_workspace(g, num_ctas):
+    wl = g.wl
+    n = kvq.kvq_decode_workspace_size(g.cache, wl.num_seqs, wl.num_q_heads, wl.max_context_len,
+                                      num_ctas)
+    ws = torch.empty(max(n, 16) // 4 + 4, dtype=torch.float32, device=g.key.device)
+    ws.view(torch.int32).random_()  # contents on entry must not matter
+    return ws
+
+
+def new_token_rows(wl):
+    """Token index of each sequence's last position (0 where the sequence is empty)."""
+    lens = wl.context_lens.astype(np.int64)
+    last = np.cumsum(lens) - 1
+    has = lens > 0
+    return np.where(has, last, 0), has
+
+
+def append_step(wl, num_ctas=0, head_scales=False):
+    """Cache write of every token but each sequence's last, then one
+    kvq_decode_append call with the last tokens; returns (GpuRun, out)."""
+    g = GpuRun(wl, head_scales=head_scales)
+    rows, has = new_token_rows(wl)
+    slots = wl.slot_mapping.copy()
+    slots[rows[has]] = -1
+    dev = g.key.device
+    kvq.kvq_write_cache(g.cache, g.key, g.value, torch.from_numpy(slots).to(dev))
+    r = torch.from_numpy(rows).to(dev)
+    new_k, new_v = g.key[r].contiguous(), g.value[r].contiguous()
+    out = torch.empty_like(g.query)
+    kvq.kvq_decode_append(g.cache, new_k, new_v, g.query, out, g.block_table, g.context_lens,
+                          wl.max_context_len, float(OA.default_sm_scale(wl.head_dim)),
+                          random_workspace(g, num_ctas), num_ctas)
+    return g, out
+
+
 def blocks_of(wl: W.Workload, seqs) -> np.ndarray:
     out = []
     for s in seqs:

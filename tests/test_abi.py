@@ -130,6 +130,31 @@ def test_decode_validation(lib):
     assert _decode(lib, d, s=0) == 0
 
 
+def _append(lib, desc, **kw):
+    a = dict(k=FAKE, v=FAKE, nk=FAKE, nv=FAKE, ks=1024, vs=1024, out=FAKE, q=FAKE, s=4, hq=32,
+             bt=FAKE, mb=64, cl=FAKE, mc=1024, sm=0.088, p=256, ws=None, wsb=0)
+    a.update(kw)
+    return lib.kvq_decode_append(ctypes.byref(desc), a["k"], a["v"], a["nk"], a["nv"], a["ks"],
+                                 a["vs"], a["out"], a["q"], a["s"], a["hq"], a["bt"], a["mb"],
+                                 a["cl"], a["mc"], a["sm"], a["p"], a["ws"], a["wsb"], None)
+
+
+def test_append_validation(lib):
+    d = _desc()
+    assert _append(lib, d, nk=None) == 1
+    assert _append(lib, d, nv=FAKE + 8) == 1  # rows are read in 16-byte pieces
+    assert _append(lib, d, ks=1016) == 1  # stride shorter than a sequence's row
+    assert _append(lib, d, vs=1028) == 1  # stride not a multiple of 8
+    assert _append(lib, _desc(head_dim=96)) == 2
+    assert _append(lib, _desc(k_fmt=4, v_fmt=1, k_meta=FAKE)) == 2  # mixed families
+    # then the decode's own checks
+    assert _append(lib, d, hq=30) == 1
+    assert _append(lib, d, mb=10) == 1
+    assert _append(lib, d, q=FAKE + 2) == 1
+    assert _append(lib, d) == 3  # needs a workspace (256 CTAs)
+    assert _append(lib, d, s=0, nk=None, nv=None) == 0  # no sequences: nothing to do
+
+
 def test_hadamard_and_calibrate_validation(lib):
     assert lib.kvq_hadamard(FAKE, 2, 10, 128, None, 0, None) == 1
     assert lib.kvq_hadamard(FAKE, 0, 10, 96, None, 0, None) == 2
