@@ -95,7 +95,7 @@ typedef struct {
   int32_t v_fmt;        /* kvq_format */
   int32_t num_kv_heads; /* >= 1 */
   int32_t head_dim;     /* 64 or 128 */
-  int32_t block_size;   /* tokens per block: 16, 32, 64 or 128 */
+  int32_t block_size;   /* tokens per block: 8, 16, 32, 64 or 128 */
   int32_t num_blocks;   /* >= 1 */
   uint32_t flags;       /* KVQ_FLAG_* */
   float k_scale;        /* symmetric K formats: > 0 (1.0 = uncalibrated fp8) */

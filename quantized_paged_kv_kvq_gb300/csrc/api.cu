@@ -35,8 +35,11 @@ kvq_status check_cache(const kvq_cache_desc* c) {
     return KVQ_ERR_INVALID_ARGUMENT;
   if (c->flags & ~KVQ_FLAG_VARNORM_ROTATE) return KVQ_ERR_INVALID_ARGUMENT;
   if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
-  if (c->block_size != 16 && c->block_size != 32 && c->block_size != 64 && c->block_size != 128)
-    return KVQ_ERR_UNSUPPORTED;  // a power of two >= 16: a 16-token tile never spans blocks
+  // a power of two from 8 to 128: a 16-token tile lies in one block, or in two
+  // consecutive entries of the block table (8-token pages)
+  if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32 && c->block_size != 64 &&
+      c->block_size != 128)
+    return KVQ_ERR_UNSUPPORTED;
   const bool kvarn = (c->flags & KVQ_FLAG_VARNORM_ROTATE) != 0;
   if (!pairing_ok(c->k_fmt, c->v_fmt, kvarn)) return KVQ_ERR_UNSUPPORTED;
   if (!is_asym(c->k_fmt) && !(c->k_scale > 0.0f && isfinite(c->k_scale)))
@@ -411,7 +414,8 @@ kvq_status kvq_get_device_error(kvq_stream_t stream, uint32_t* bits) {
   if (bits == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return KVQ_ERR_CUDA;
   unsigned v = 0;
-  cudaError_t (*take[])(unsigned*) = {take_error_bits_write, take_error_bits_decode_d64_sym,
+  cudaError_t (*take[])(unsigned*) = {take_error_bits_write, take_error_bits_write_asym,
+                                      take_error_bits_decode_d64_sym,
                                       take_error_bits_decode_d128_sym,
                                       take_error_bits_decode_d64_asym,
                                       take_error_bits_decode_d128_asym};

@@ -68,13 +68,18 @@ struct DecodeCfg {
   static constexpr int V_SWZ = swz_bits(VB);
   static constexpr int align(int x) { return (x + 1023) / 1024 * 1024; }
   static constexpr int align128(int x) { return (x + 127) / 128 * 128; }
+  // metadata of one field set: room for two 8-token boxes (pages of 8 tokens)
+  // or one 16-token box
+  static constexpr int meta_half(int hpc, int f) { return align128(hpc * f * 16); }
+  static constexpr int meta_room(int hpc, int f) { return 2 * meta_half(hpc, f); }
   static constexpr int stage_bytes(int hpc) {
-    return align(hpc * K_HEAD) + align(hpc * V_HEAD) + align(align128(hpc * KMF * 32) + hpc * VMF * 32);
+    return align(hpc * K_HEAD) + align(hpc * V_HEAD) + align(meta_room(hpc, KMF) + meta_room(hpc, VMF));
   }
   static constexpr int STAGE_MAX = stage_bytes(kHeadsPerCta);
   static constexpr int STAGES = STAGE_MAX >= 24576 ? 3 : STAGE_MAX >= 16384 ? 5 : 6;
   static constexpr bool KVARN_ = KVARN;
   static_assert(KW * 4 == K_LANE && VW * 4 == VPS, "layout");
+  static_assert(KMF == VMF || KMF == 0 || VMF == 0, "one metadata row layout for K and V");
 };
 
 // Shared memory of a CTA (bytes): the ring; per warp its query rows (G rows of
@@ -122,11 +127,16 @@ __device__ __forceinline__ void k_frag(const uint32_t (&kw)[2][KW], int j, uint3
                                        uint32_t& a1, uint32_t& a2, uint32_t& a3) {
   constexpr uint32_t K64 = 0x64646464u;
   if constexpr (KF == INT4A) {
-    const int m = j >> 1, sh = (j & 1) * 8;
-    a0 = and_or(kw[0][m] >> sh, 0x000F000Fu, 0x64006400u);
-    a2 = and_or(kw[0][m] >> (sh + 4), 0x000F000Fu, 0x64006400u);
-    a1 = and_or(kw[1][m] >> sh, 0x000F000Fu, 0x64006400u);
-    a3 = and_or(kw[1][m] >> (sh + 4), 0x000F000Fu, 0x64006400u);
+    // low nibble of each byte pair -> 1024 + c (0x6400 | c), high nibble in
+    // place -> 64 + c (0x5400 | c << 4, where one fp16 step is 1/16): one shift
+    // per word; the two offsets come off after the k-sum
+    const int m = j >> 1;
+    const uint32_t w0 = (j & 1) ? (kw[0][m] >> 8) : kw[0][m];
+    const uint32_t w1 = (j & 1) ? (kw[1][m] >> 8) : kw[1][m];
+    a0 = and_or(w0, 0x000F000Fu, 0x64006400u);
+    a2 = and_or(w0, 0x00F000F0u, 0x54005400u);
+    a1 = and_or(w1, 0x000F000Fu, 0x64006400u);
+    a3 = and_or(w1, 0x00F000F0u, 0x54005400u);
   } else if constexpr (KF == E4M3) {
     a0 = e4m3x2_to_f16x2(kw[0][j] & 0xFFFFu);
     a2 = e4m3x2_to_f16x2(kw[0][j] >> 16);
@@ -150,11 +160,11 @@ template <int VF>
 __device__ __forceinline__ void v_pair(uint32_t wa, uint32_t wb, int i, uint32_t& rg,
                                        uint32_t& rg8) {
   constexpr uint32_t K64 = 0x64646464u;
-  if constexpr (VF == INT4A) {
+  if constexpr (VF == INT4A) {  // (1024 + c) - 1024 and (64 + c) - 64, exact
     const uint32_t pr = (i & 2) ? prmt(wa, wb, 0x7632) : prmt(wa, wb, 0x5410);
-    const int sh = (i & 1) * 8;
-    rg = hsub2_u32(and_or(pr >> sh, 0x000F000Fu, 0x64006400u), 0x64006400u);
-    rg8 = hsub2_u32(and_or(pr >> (sh + 4), 0x000F000Fu, 0x64006400u), 0x64006400u);
+    const uint32_t w = (i & 1) ? (pr >> 8) : pr;
+    rg = hsub2_u32(and_or(w, 0x000F000Fu, 0x64006400u), 0x64006400u);
+    rg8 = hsub2_u32(and_or(w, 0x00F000F0u, 0x54005400u), 0x54005400u);
   } else {
     const uint32_t il = (i & 1) ? prmt(wa, wb, 0x7362) : prmt(wa, wb, 0x5140);
     if constexpr (VF == E4M3) {
@@ -335,6 +345,8 @@ struct Cursor {
   int i;           // loads issued
 };
 
+static_assert(sizeof(Cursor) <= 40, "the cursor lives in scratch words 16..20");
+
 struct DecodeMaps {
   CUtensorMap k, v, km, vm;
 };
@@ -488,6 +500,9 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long 
         float bm = ml[0][0];
 #pragma unroll
         for (int u = 1; u < PU; ++u) bm = fmaxf(bm, ml[u][0]);
+        // no slot in this batch (empty ranges; more ranges than tiles): nothing to
+        // add, and 2^(m - M) would be 2^(-inf + inf) while M is still -inf
+        if (bm == -INFINITY) continue;
         if (bm > M) {  // raise the running maximum, rescaling what was summed so far
           const float sc = fast_exp2(M - bm);
           Lsum *= sc;
@@ -613,6 +628,9 @@ __device__ __forceinline__ void merge_slots(const DecodeArgs& a, int s, long lon
         float bm = ml[0][0];
 #pragma unroll
         for (int u = 1; u < PU; ++u) bm = fmaxf(bm, ml[u][0]);
+        // no slot in this batch (empty ranges; more ranges than tiles): nothing to
+        // add, and 2^(m - M) would be 2^(-inf + inf) while M is still -inf
+        if (bm == -INFINITY) continue;
         if (bm > M) {  // raise the running maximum, rescaling what was summed so far
           const float sc = fast_exp2(M - bm);
           Lsum *= sc;
@@ -754,7 +772,9 @@ __device__ __forceinline__ void append_new_tokens(const DecodeArgs& a, long long
 // range of such a sequence merges the slots.  Store-then-fence-then-load of
 // the tags guarantees at least one finder; a claim word per sequence keeps it
 // to one.
-template <int D, int KF, int VF, bool KVARN>
+// SPLIT: pages of 8 tokens (a tile is two pages); a separate instance, so that
+// the other page sizes keep the one-box path's registers.
+template <int D, int KF, int VF, bool KVARN, bool SPLIT>
 __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     decode_partition_kernel(const DecodeArgs a, const __grid_constant__ DecodeMaps maps) {
   using C = DecodeCfg<D, KF, VF, KVARN>;
@@ -773,7 +793,9 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
   const int stage_bytes = C::stage_bytes(hpc);
   const int v_off = C::align(hpc * C::K_HEAD);
   const int m_off = v_off + C::align(hpc * C::V_HEAD);  // K metadata box, then V's
-  const int vm_off = m_off + C::align128(hpc * C::KMF * 32);
+  const int vm_off = m_off + C::meta_room(hpc, C::KMF);
+  // 8-token pages: a 16-token tile is two pages, loaded as two boxes each
+  constexpr bool split = SPLIT;
   const uint32_t ring_end = C::STAGES * stage_bytes;
   const int qrb = q_rows_bytes(G, D);
   const uint32_t qbuf_s = base_s + ring_end + warp * qrb;  // this warp's query rows (bf16)
@@ -899,8 +921,19 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
   // The cursor lives in shared memory: only thread 0 uses it, and registers
   // held by every thread for it would be taken from the consumers.
   Cursor* cur = reinterpret_cast<Cursor*>(scratch + 16);
+  // 8-token pages: block id of the cursor tile's second page (read ahead); kept
+  // out of the cursor, whose copies stay as small as for the other page sizes
+  int* const cur_blk2 = reinterpret_cast<int*>(scratch + 21);
   auto block_of = [&](const Cursor& u) {  // block id of the cursor's tile
     return a.block_table[static_cast<size_t>(u.s) * a.max_blocks_per_seq + ((16 * u.t) >> bs_shift)];
+  };
+  auto second_half = [&](const Cursor& u) {  // 8-token pages: tokens 8..15 of the tile exist
+    return split && 16 * u.t + 8 < u.ctx;
+  };
+  auto block2_of = [&](const Cursor& u) {  // their page (entries past the context are never read)
+    return second_half(u) ? a.block_table[static_cast<size_t>(u.s) * a.max_blocks_per_seq +
+                                          ((16 * u.t) >> bs_shift) + 1]
+                          : 0;
   };
   auto find_next = [&](Cursor& u) {  // first sequence after u.s with tokens, if the range goes on
     u.nx = S;
@@ -923,6 +956,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     u.ctx = min(a.context_lens[s_first], a.max_context_len);
     u.tiles = (u.ctx + 15) >> 4;
     u.blk = block_of(u);
+    if constexpr (split) *cur_blk2 = block2_of(u);
     u.nx_ctx = 0;
     u.i = 0;
     find_next(u);
@@ -948,18 +982,45 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     const int off = tok & bs_mask;
     const uint32_t sb = base_s + st * stage_bytes;
     const uint32_t bar = full_s + 8 * st;
-    mbar_arrive_expect(bar, tile_bytes);
-    if (a.one_box) {
-      tma_load_4d(sb, &maps.k, 0, off, hg * hpc, blk, bar, pol);
-      tma_load_4d(sb + v_off, &maps.v, 0, off, hg * hpc, blk, bar, pol);
-    } else {
-      for (int hh = 0; hh < hpc; ++hh) {
-        tma_load_4d(sb + hh * C::K_HEAD, &maps.k, 0, hg * hpc + hh, off, blk, bar, pol);
-        tma_load_4d(sb + v_off + hh * C::V_HEAD, &maps.v, 0, hg * hpc + hh, off, blk, bar, pol);
+    if constexpr (split) {  // 8-token pages: the tile is two pages, each loaded as
+      // per-head 8-row boxes (rows 0-7, then 8-15 of the head's [16][row] box)
+      // and [head][field][8] metadata boxes (the second meta_half bytes on)
+      const bool two = second_half(u);
+      int blk2 = *cur_blk2;
+      if (two && (blk2 < 0 || blk2 >= a.num_blocks)) {
+        raise_error(2u);
+        blk2 = 0;
       }
+      mbar_arrive_expect(bar, two ? tile_bytes : tile_bytes / 2);
+      for (int hf = 0; hf < (two ? 2 : 1); ++hf) {
+        const int b = hf ? blk2 : blk;
+        for (int hh = 0; hh < hpc; ++hh) {
+          tma_load_4d(sb + hh * C::K_HEAD + hf * 8 * C::KB, &maps.k, 0, hg * hpc + hh, 0, b, bar,
+                      pol);
+          tma_load_4d(sb + v_off + hh * C::V_HEAD + hf * 8 * C::VB, &maps.v, 0, hg * hpc + hh, 0, b,
+                      bar, pol);
+        }
+        if constexpr (C::KMF > 0)
+          tma_load_4d(sb + m_off + hf * C::meta_half(hpc, C::KMF), &maps.km, 0, 0, hg * hpc, b, bar,
+                      pol);
+        if constexpr (C::VMF > 0)
+          tma_load_4d(sb + vm_off + hf * C::meta_half(hpc, C::VMF), &maps.vm, 0, 0, hg * hpc, b,
+                      bar, pol);
+      }
+    } else {  // one box per tile (pages of 16 or more tokens)
+      mbar_arrive_expect(bar, tile_bytes);
+      if (a.one_box) {
+        tma_load_4d(sb, &maps.k, 0, off, hg * hpc, blk, bar, pol);
+        tma_load_4d(sb + v_off, &maps.v, 0, off, hg * hpc, blk, bar, pol);
+      } else {
+        for (int hh = 0; hh < hpc; ++hh) {
+          tma_load_4d(sb + hh * C::K_HEAD, &maps.k, 0, hg * hpc + hh, off, blk, bar, pol);
+          tma_load_4d(sb + v_off + hh * C::V_HEAD, &maps.v, 0, hg * hpc + hh, off, blk, bar, pol);
+        }
+      }
+      if constexpr (C::KMF > 0) tma_load_4d(sb + m_off, &maps.km, off, 0, hg * hpc, blk, bar, pol);
+      if constexpr (C::VMF > 0) tma_load_4d(sb + vm_off, &maps.vm, off, 0, hg * hpc, blk, bar, pol);
     }
-    if constexpr (C::KMF > 0) tma_load_4d(sb + m_off, &maps.km, off, 0, hg * hpc, blk, bar, pol);
-    if constexpr (C::VMF > 0) tma_load_4d(sb + vm_off, &maps.vm, off, 0, hg * hpc, blk, bar, pol);
     ++u.i;
     if (++u.t == u.tiles && u.i < n) {  // on to the next sequence with tokens
       u.ps += u.tiles;
@@ -974,7 +1035,10 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
       u.tiles = (u.ctx + 15) >> 4;
       find_next(u);
     }
-    if (u.i < n) u.blk = block_of(u);  // prefetched: consumed by the next issue
+    if (u.i < n) {  // prefetched: consumed by the next issue
+      u.blk = block_of(u);
+      if constexpr (split) *cur_blk2 = block2_of(u);
+    }
     *cur = u;
   };
   if (threadIdx.x == 0)
@@ -994,8 +1058,14 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
   for (int u = 0; u < 4; ++u)
     v_addr[u] = v_off + swz_addr<C::VB, C::V_SWZ>(warp * C::V_HEAD, v_token(c, u),
                                                   (g * C::VPS) / 16, (g * C::VPS) % 16);
-  const uint32_t meta_k = m_off + warp * C::KMF * 32;
-  const uint32_t meta_v = vm_off + warp * C::VMF * 32;
+  // metadata rows: per warp [field][16 tokens]; with 8-token pages two boxes of
+  // [warp][field][8 tokens], the second meta_half bytes on
+  constexpr int fstr = split ? 16 : 32;  // bytes between a warp's fields
+  const int mhalf = C::meta_half(hpc, C::KMF > 0 ? C::KMF : C::VMF);
+  const uint32_t mrow0 = split ? (row0 >> 3) * mhalf + 2 * (row0 & 7) : 2 * row0;
+  const uint32_t mrow1 = split ? (row1 >> 3) * mhalf + 2 * (row1 & 7) : 2 * row1;
+  const uint32_t meta_k = m_off + warp * C::KMF * fstr;
+  const uint32_t meta_v = vm_off + warp * C::VMF * fstr;
   // this warp's kv-head scales (per-kv-head scales, when given, replace the tensor's)
   const float vsc = is_asym(VF) ? 1.0f : (a.v_head_scale != nullptr ? a.v_head_scale[h] : a.v_scale);
   const float qks = (!is_asym(KF) && a.k_head_scale != nullptr) ? a.qk_base * a.k_head_scale[h]
@@ -1003,6 +1073,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
 
   uint32_t qf[C::KSTEPS][2];
   float qsum0 = 0.f, qsum1 = 0.f;
+  float qb0 = 0.f, qb1 = 0.f;  // int4 K: sum over k of q_k times the code offset of slot k
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
   // PV accumulators as the output runs they become: lane (g, c) holds dims
   // g*E .. g*E+E-1 of query heads 2c (Oa) and 2c+1 (Ob)
@@ -1023,7 +1094,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     if (hd.flags & 1) {  // a new segment: this warp's query fragment, fresh state
       cp_async_wait<0>();  // the rows were fetched during the previous segment
       __syncwarp();
-      float qs = 0.0f;
+      float qs = 0.0f, qh = 0.0f;  // qh: the k-slots that meet high nibbles (int4 K)
       if constexpr (KVARN) {
         float* srow = reinterpret_cast<float*>(smem + rot_off + warp * D * 4);
         float qv[C::KSTEPS][4];
@@ -1047,6 +1118,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
           for (int e = 0; e < 4; ++e) {
             v[e] = g < G ? __half2float(__float2half_rn(qv[j][e])) : 0.0f;
             qs += v[e];
+            if (e >= 2) qh += v[e];
           }
           qf[j][0] = pack_half2(v[0], v[1]);
           qf[j][1] = pack_half2(v[2], v[3]);
@@ -1062,6 +1134,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
               v[e] = __half2float(__float2half_rn(__uint_as_float(
                   static_cast<uint32_t>(lds_u16(qbuf_s + 2 * (g * D + kslot_d<D, KF>(c, j, e)))) << 16)));
             qs += v[e];
+            if (e >= 2) qh += v[e];
           }
           qf[j][0] = pack_half2(v[0], v[1]);
           qf[j][1] = pack_half2(v[2], v[3]);
@@ -1073,6 +1146,15 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
       qs += __shfl_xor_sync(0xffffffffu, qs, 2);
       qsum0 = __shfl_sync(0xffffffffu, qs, (2 * c) * 4);
       qsum1 = __shfl_sync(0xffffffffu, qs, (2 * c + 1) * 4);
+      if constexpr (KF == INT4A) {  // offsets 1024 (low nibbles) and 64 (high nibbles)
+        qh += __shfl_xor_sync(0xffffffffu, qh, 1);
+        qh += __shfl_xor_sync(0xffffffffu, qh, 2);
+        qb0 = fmaf(1024.0f, qsum0, -960.0f * __shfl_sync(0xffffffffu, qh, (2 * c) * 4));
+        qb1 = fmaf(1024.0f, qsum1, -960.0f * __shfl_sync(0xffffffffu, qh, (2 * c + 1) * 4));
+      } else {
+        qb0 = 1024.0f * qsum0;
+        qb1 = 1024.0f * qsum1;
+      }
       m0 = m1 = -INFINITY;
       l0 = l1 = z0 = z1 = 0.f;
 #pragma unroll
@@ -1100,10 +1182,10 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     float ks0 = 1.f, ks1 = 1.f, kz0 = 0.f, kz1 = 0.f, vs0 = 1.f, vs1 = 1.f, vz0 = 0.f, vz1 = 0.f;
     if constexpr (is_asym(KF)) {
       const uint32_t mk = sb + meta_k;
-      ks0 = lds_half(mk + 2 * row0); ks1 = lds_half(mk + 2 * row1);
-      kz0 = lds_half(mk + 32 + 2 * row0); kz1 = lds_half(mk + 32 + 2 * row1);
+      ks0 = lds_half(mk + mrow0); ks1 = lds_half(mk + mrow1);
+      kz0 = lds_half(mk + fstr + mrow0); kz1 = lds_half(mk + fstr + mrow1);
       if constexpr (KVARN) {
-        const float sg0 = lds_half(mk + 64 + 2 * row0), sg1 = lds_half(mk + 64 + 2 * row1);
+        const float sg0 = lds_half(mk + 2 * fstr + mrow0), sg1 = lds_half(mk + 2 * fstr + mrow1);
         ks0 *= sg0; kz0 *= sg0; ks1 *= sg1; kz1 *= sg1;
       }
     }
@@ -1134,10 +1216,10 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
         sl[2] = (sacc[2] - bias * qsum0) * qks;
         sl[3] = (sacc[3] - bias * qsum1) * qks;
       } else {
-        sl[0] = (ks0 * (sacc[0] - 1024.0f * qsum0) + kz0 * qsum0) * a.qk_scale;
-        sl[1] = (ks0 * (sacc[1] - 1024.0f * qsum1) + kz0 * qsum1) * a.qk_scale;
-        sl[2] = (ks1 * (sacc[2] - 1024.0f * qsum0) + kz1 * qsum0) * a.qk_scale;
-        sl[3] = (ks1 * (sacc[3] - 1024.0f * qsum1) + kz1 * qsum1) * a.qk_scale;
+        sl[0] = (ks0 * (sacc[0] - qb0) + kz0 * qsum0) * a.qk_scale;
+        sl[1] = (ks0 * (sacc[1] - qb1) + kz0 * qsum1) * a.qk_scale;
+        sl[2] = (ks1 * (sacc[2] - qb0) + kz1 * qsum0) * a.qk_scale;
+        sl[3] = (ks1 * (sacc[3] - qb1) + kz1 * qsum1) * a.qk_scale;
       }
     }
     const bool ok0 = row0 < valid, ok1 = row1 < valid;
@@ -1160,10 +1242,10 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     }
     if constexpr (is_asym(VF)) {
       const uint32_t mv = sb + meta_v;
-      vs0 = lds_half(mv + 2 * row0); vs1 = lds_half(mv + 2 * row1);
-      vz0 = lds_half(mv + 32 + 2 * row0); vz1 = lds_half(mv + 32 + 2 * row1);
+      vs0 = lds_half(mv + mrow0); vs1 = lds_half(mv + mrow1);
+      vz0 = lds_half(mv + fstr + mrow0); vz1 = lds_half(mv + fstr + mrow1);
       if constexpr (KVARN) {
-        const float sg0 = lds_half(mv + 64 + 2 * row0), sg1 = lds_half(mv + 64 + 2 * row1);
+        const float sg0 = lds_half(mv + 2 * fstr + mrow0), sg1 = lds_half(mv + 2 * fstr + mrow1);
         vs0 *= sg0; vz0 *= sg0; vs1 *= sg1; vz1 *= sg1;
       }
     }

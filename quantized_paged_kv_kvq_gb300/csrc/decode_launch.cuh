@@ -31,13 +31,13 @@ inline CUtensorMapSwizzle swizzle_mode(int bits) {
 }
 
 // Codes [NB, bs, Hkv, row] bytes: dims (row, Hkv, bs, NB), box = one head's
-// 16 tokens.
+// 16 tokens (8 with 8-token pages: one page).
 inline bool encode_codes_map(CUtensorMap* m, const void* base, int row, int hkv, int bs, int nb,
                              int swz_bits) {
   const cuuint64_t dims[4] = {cuuint64_t(row), cuuint64_t(hkv), cuuint64_t(bs), cuuint64_t(nb)};
   const cuuint64_t strides[3] = {cuuint64_t(row), cuuint64_t(row) * hkv,
                                  cuuint64_t(row) * hkv * bs};
-  const cuuint32_t box[4] = {cuuint32_t(row), 1, 16, 1};
+  const cuuint32_t box[4] = {cuuint32_t(row), 1, cuuint32_t(bs < 16 ? bs : 16), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -62,13 +62,14 @@ inline bool encode_codes_map_headmajor(CUtensorMap* m, const void* base, int row
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Metadata [NB, Hkv, F, bs] fp16: dims (bs, F, Hkv, NB), box = 16 tokens x F x hpc.
+// Metadata [NB, Hkv, F, bs] fp16: dims (bs, F, Hkv, NB), box = 16 tokens x F x hpc
+// (8 tokens with 8-token pages).
 inline bool encode_meta_map(CUtensorMap* m, const void* base, int nf, int hkv, int bs, int nb,
                             int hpc) {
   const cuuint64_t dims[4] = {cuuint64_t(bs), cuuint64_t(nf), cuuint64_t(hkv), cuuint64_t(nb)};
   const cuuint64_t strides[3] = {cuuint64_t(bs) * 2, cuuint64_t(bs) * 2 * nf,
                                  cuuint64_t(bs) * 2 * nf * hkv};
-  const cuuint32_t box[4] = {16, cuuint32_t(nf), cuuint32_t(hpc), 1};
+  const cuuint32_t box[4] = {cuuint32_t(bs < 16 ? bs : 16), cuuint32_t(nf), cuuint32_t(hpc), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -84,7 +85,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   memset(&maps, 0, sizeof(maps));
   const int hpc = a.heads_per_cta;
   DecodeArgs args = a;
-  args.one_box = encode_codes_map_headmajor(&maps.k, a.k_cache, C::KB, a.num_kv_heads,
+  // (8-token pages take per-head boxes: two land as one head's 16 rows)
+  args.one_box = a.block_size >= 16 &&
+                 encode_codes_map_headmajor(&maps.k, a.k_cache, C::KB, a.num_kv_heads,
                                             a.block_size, a.num_blocks, hpc, C::K_SWZ) &&
                  encode_codes_map_headmajor(&maps.v, a.v_cache, C::VB, a.num_kv_heads,
                                             a.block_size, a.num_blocks, hpc, C::V_SWZ);
@@ -101,7 +104,9 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
                                      a.num_blocks, hpc))
     return cudaErrorInvalidValue;
 
-  auto kern = decode_partition_kernel<D, KF, VF, KVARN>;
+  auto kern_one = decode_partition_kernel<D, KF, VF, KVARN, false>;
+  auto kern_split = decode_partition_kernel<D, KF, VF, KVARN, true>;  // 8-token pages
+  auto kern = a.block_size < 16 ? kern_split : kern_one;
   const int smem = decode_smem_bytes<C>(hpc, a.gqa);
   static std::atomic<unsigned long long> attr_done{0};  // one bit per device
   int dev = 0;
@@ -109,9 +114,11 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_done.load() & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             decode_smem_bytes<C>(kHeadsPerCta, 8));
-    if (e != cudaSuccess) return e;
+    for (auto k : {kern_one, kern_split}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               decode_smem_bytes<C>(kHeadsPerCta, 8));
+      if (e != cudaSuccess) return e;
+    }
     attr_done.fetch_or(bit);
   }
   const dim3 grid(a.num_ctas, a.num_kv_heads / hpc, 1);

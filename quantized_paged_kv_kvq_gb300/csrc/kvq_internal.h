@@ -85,6 +85,8 @@ struct DecodeArgs {
 
 cudaError_t launch_write(const WriteArgs& a, int head_dim, int kf, int vf, bool kvarn,
                          cudaStream_t st);
+cudaError_t launch_write_asym(const WriteArgs& a, int head_dim, int kf, int vf, bool kvarn,
+                              cudaStream_t st);
 bool write_supported(int kf, int vf, bool kvarn);
 
 cudaError_t launch_decode_d64_sym(const DecodeArgs& a, int kf, int vf, cudaStream_t st);
@@ -96,6 +98,7 @@ cudaError_t launch_decode_d128_asym(const DecodeArgs& a, int kf, int vf, bool kv
 
 // read-and-clear of each translation unit's device error word
 cudaError_t take_error_bits_write(unsigned* bits);
+cudaError_t take_error_bits_write_asym(unsigned* bits);
 cudaError_t take_error_bits_decode_d64_sym(unsigned* bits);
 cudaError_t take_error_bits_decode_d128_sym(unsigned* bits);
 cudaError_t take_error_bits_decode_d64_asym(unsigned* bits);

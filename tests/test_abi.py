@@ -68,7 +68,8 @@ def test_write_validation(lib):
     ok_desc = _desc()
     assert _write(lib, None) == 1
     assert _write(lib, _desc(head_dim=96)) == 2
-    assert _write(lib, _desc(block_size=8)) == 2
+    assert _write(lib, _desc(block_size=4)) == 2
+    assert _write(lib, _desc(block_size=24)) == 2
     assert _write(lib, _desc(k_fmt=9)) == 1
     assert _write(lib, _desc(k_scale=0.0)) == 1
     assert _write(lib, _desc(k_scale=float("nan"))) == 1

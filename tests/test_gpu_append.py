@@ -97,7 +97,7 @@ def test_append_equals_write_then_decode(name, ctas):
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
 
-@pytest.mark.parametrize("bs", [32, 64, 128])
+@pytest.mark.parametrize("bs", [8, 32, 64, 128])
 def test_append_block_sizes(bs):
     wl = W.workload("llama8b_int8", num_seqs=5, ctx_lo=1, ctx_hi=600, block_size=bs)
     g, out = append_step(wl, num_ctas=0)

@@ -91,13 +91,13 @@ def test_block_permutation_gives_identical_output():
     assert torch.equal(out1, out2)
 
 
-@pytest.mark.parametrize("name", ["llama8b_int8", "kvarn_131k"])
+@pytest.mark.parametrize("name", ["llama8b_int8", "kvarn_131k", "llama70b_int4"])
 def test_block_sizes_agree(name):
-    """Pages of 16, 32, 64 and 128 tokens: codes bit-exact with the oracle's
+    """Pages of 8, 16, 32, 64 and 128 tokens: codes bit-exact with the oracle's
     cache of the same page size, outputs within tolerance and alike."""
     lens = np.array([33, 100, 257, 5, 300], np.int32)
     outs = []
-    for bs in (16, 32, 64, 128):
+    for bs in (8, 16, 32, 64, 128):
         wl = W.workload(name, num_seqs=len(lens), context_lens=lens, block_size=bs)
         g = GpuRun(wl)
         g.write()
@@ -111,6 +111,37 @@ def test_block_sizes_agree(name):
             assert_attention_close(outs[-1], o.decode(), f"{name} bs={bs} ctas={ctas}")
     for other in outs[1:]:
         assert_attention_close(outs[0], other, f"{name}: page sizes")
+    assert kvq.kvq_get_device_error() == 0
+
+
+SMALL_PAGE_SHAPES = {
+    "int8_d64_2heads": ("tiny_int8", {}),
+    "int4_d64_2heads": ("llama70b_int4", dict(num_q_heads=8, num_kv_heads=2, head_dim=64)),
+    "kvarn_d128_2heads": ("kvarn_131k", dict(num_q_heads=8, num_kv_heads=2)),
+    "fp8_d128_4heads": ("llama8b_e4m3k_int8v", dict(num_q_heads=16, num_kv_heads=4)),
+}
+
+
+@pytest.mark.parametrize("shape", list(SMALL_PAGE_SHAPES))
+@pytest.mark.parametrize("bs", [8, 16])
+def test_small_pages_few_heads(shape, bs):
+    """8-token pages (a tile spans two pages; the second may be absent) and
+    16-token pages with fewer than 8 kv-heads per CTA, around page edges."""
+    name, kw = SMALL_PAGE_SHAPES[shape]
+    lens = np.array([1, 7, 8, 9, 15, 16, 17, 24, 25, 0, 100, 333], np.int32)
+    wl = W.workload(name, **dict(kw, num_seqs=len(lens), context_lens=lens, block_size=bs))
+    g = GpuRun(wl)
+    g.write()
+    o = OracleRun(wl)
+    kc, km, vc, vm = g.cache_numpy()
+    assert np.array_equal(kc, o.kc) and np.array_equal(vc, o.vc), f"{shape} bs={bs}: codes"
+    if km is not None:
+        assert np.array_equal(km, o.km) and np.array_equal(vm, o.vm), f"{shape} bs={bs}: meta"
+    ref = o.decode()
+    for ctas in (1, 5, 0):
+        got = out_numpy(g.decode(num_ctas=ctas))
+        assert np.all(got[lens == 0] == 0)
+        assert_attention_close(got, ref, f"{shape} bs={bs} ctas={ctas}")
     assert kvq.kvq_get_device_error() == 0
 
 
