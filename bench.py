@@ -37,6 +37,7 @@ DECODE_SOURCES = ["decode.cuh", "decode_launch.cuh", "kvq_device.cuh", "quant_ro
                   "decode_d128_sym.cu", "decode_d128_asym.cu", "decode_d64_sym.cu",
                   "decode_d64_asym.cu"]
 WRITE_SOURCES = ["write.cu", "kvq_device.cuh", "quant_row.cuh"]
+WRITE_ASYM_SOURCES = ["write_asym.cu", "kvq_device.cuh", "quant_row.cuh"]
 
 
 def parse_args(argv=None):
@@ -120,6 +121,8 @@ def profiled_traffic(workload: str, kernel: str = "decode_partition"):
                 vals[k.strip()] = v.strip().strip("`")
     if kernel == "decode_partition":
         ok = vals.get("decode_source_sha256_16") == decode_source_hash()
+    elif kernel == "write_asym":
+        ok = vals.get("write_source_sha256_16") == source_hash(WRITE_ASYM_SOURCES)
     else:
         ok = vals.get("write_source_sha256_16") == source_hash(WRITE_SOURCES)
     if not ok:
@@ -439,9 +442,10 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
                  "peak": hbm, "peak_source": peak_note, "unit": "GB/s", "frac": achieved / hbm,
                  "traffic": profiled_traffic(args.workload, "decode_partition"),
                  "algorithmic_bytes": dbytes}
-    rl_write = {"bound": "hbm", "kernel": "write_cache_kernel", "achieved": achieved_w,
+    wkern = "write_asym" if wl.k_fmt.endswith("_asym") else "write_cache"
+    rl_write = {"bound": "hbm", "kernel": wkern + "_kernel", "achieved": achieved_w,
                 "peak": hbm, "peak_source": peak_note, "unit": "GB/s", "frac": achieved_w / hbm,
-                "traffic": profiled_traffic(args.workload, "write_cache"),
+                "traffic": profiled_traffic(args.workload, wkern),
                 "algorithmic_bytes": wbytes}
 
     # one decode step that brings its own token (one per sequence): the fused
