@@ -51,6 +51,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--chunk-tokens", type=int, default=16384,
+                   help="prefill-chunk write timed when sequence 0 is at least this long (0: off)")
     p.add_argument("--no-append", action="store_true",
                    help="skip the fused append-and-decode step timing")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -489,6 +491,35 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
                     "write_then_decode_us": res["unfused"], "steps": n_app,
                     "stat": "median, L2 flushed before each step", "tokens_per_step": int(has.sum())}
 
+    # a prefill chunk: the write of `chunk_tokens` new tokens into sequence 0's
+    # pages (the long-context shape's prefill step), L2 flushed before each
+    chunk = None
+    C = args.chunk_tokens
+    if C > 0 and int(wl.context_lens[0]) >= C:
+        pc = W.prefill_chunk(wl, C, seed=W.SEEDS[args.workload] + 7 + 100 * rank)
+        ck, cv = bf(pc["key"]), bf(pc["value"])
+        cs = torch.from_numpy(pc["slot_mapping"]).to(dev)
+        n_ch = max(3, min(K, 200))
+
+        def chunk_write(ev):
+            flush_l2()
+            ev[0].record()
+            kvq.kvq_write_cache(cache, ck, cv, cs)
+            ev[1].record()
+
+        for _ in range(3):
+            chunk_write(mk())
+        evs = [mk() for _ in range(n_ch)]
+        for ev in evs:
+            chunk_write(ev)
+        torch.cuda.synchronize()
+        us = max_over_ranks([float(np.median([e[0].elapsed_time(e[1]) for e in evs])) * 1e3],
+                            dev)[0]
+        cbytes = C * (2 * wl.num_kv_heads * wl.head_dim * 2 + kv_bytes_per_token(wl) + 8)
+        chunk = {"tokens": C, "us": us, "tok_s": C / us * 1e6, "gbs": cbytes / us / 1e3,
+                 "frac_of_hbm": cbytes / us / 1e3 / hbm, "steps": n_ch,
+                 "stat": "median, L2 flushed before each write"}
+
     # end to end through the public API: pinned host inputs in, result out
     e2e = None
     if not args.no_e2e:
@@ -557,6 +588,7 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
         "decode_frac_of_hbm": gbs / world / hbm,
         "e2e": e2e,
         "decode_step_append": step_lat,
+        "prefill_chunk_write": chunk,
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,

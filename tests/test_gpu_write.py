@@ -173,3 +173,25 @@ def test_per_head_scales_calibration_and_codes_bit_exact(name):
     kc, _, vc, _ = g.cache_numpy()
     assert np.array_equal(kc, o.kc) and np.array_equal(vc, o.vc)
     assert kvq.kvq_get_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["kvarn_131k", "llama8b_int8"])
+def test_prefill_chunk_write_bit_exact(name):
+    """A prefill chunk (new tokens over sequence 0's first pages, as the long-context
+    shape's chunked prefill writes them) lands bit-exact over an existing cache."""
+    wl = W.workload(name, num_seqs=2, ctx_lo=3000, ctx_hi=3000)
+    pc = W.prefill_chunk(wl, 2048, seed=5)
+    g = GpuRun(wl)
+    o = OracleRun(wl)
+    g.write()
+    kvq.kvq_write_cache(g.cache, bf16(pc["key"]), bf16(pc["value"]),
+                        torch.from_numpy(pc["slot_mapping"]).cuda())
+    for codes, meta, x, fmt, sc in ((o.kc, o.km, pc["key"], wl.k_fmt, o.k_scale),
+                                    (o.vc, o.vm, pc["value"], wl.v_fmt, o.v_scale)):
+        OC.write_cache(codes, meta, x, pc["slot_mapping"], wl.block_size, fmt, sc, wl.kvarn,
+                       wl.signs)
+    kc, km, vc, vm = g.cache_numpy()
+    assert np.array_equal(kc, o.kc) and np.array_equal(vc, o.vc)
+    if o.km.shape[2]:
+        assert np.array_equal(km, o.km) and np.array_equal(vm, o.vm)
+    assert kvq.kvq_get_device_error() == 0
