@@ -250,6 +250,55 @@ def cpu_baseline_subprocess(workload: str, budget_s: float):
             "decode_seconds": round(tdec, 3), "write_seconds": round(twr, 3)}
 
 
+def cpu_model() -> str:
+    import platform
+    part = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+                if key == "cpu part" and part is None:  # Arm: implementer-specific part id
+                    part = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    name = platform.processor() or platform.machine()
+    return f"{name} (CPU part {part})" if part else name
+
+
+def cpu_baseline_all_cores(workload: str, budget_s: float, procs: int):
+    """The same oracle sample in `procs` concurrent single-threaded processes (one per
+    host core, each on its own seeded copy of the workload); the rate is the sum of
+    the processes' rates, each measured in its own CPU time."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    children = []
+    for i in range(procs):
+        code = ("import json,bench;r=bench.oracle_sample(%r,%d,%r);print(json.dumps(r))"
+                % (workload, 1 + i, budget_s))
+        children.append(subprocess.Popen([sys.executable, "-c", code], cwd=ROOT, env=env,
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True))
+    rate, done = 0.0, 0
+    for c in children:
+        try:
+            out, _ = c.communicate(timeout=600)
+        except subprocess.TimeoutExpired:
+            c.kill()
+            continue
+        if c.returncode != 0 or not out.strip():
+            continue
+        kv, tdec, _, _, _ = json.loads(out.strip().splitlines()[-1])
+        if tdec > 0:
+            rate += kv / tdec
+            done += 1
+    if done == 0:
+        return None
+    return {"value": round(rate / 1e9, 6), "unit": "GB/s", "cores": done,
+            "sample": f"{done} concurrent single-thread processes, each as the one-core sample",
+            "cpu_model": cpu_model()}
+
+
 def run_reference(args, rank: int):
     if rank != 0:
         return
@@ -559,6 +608,10 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
         return
     cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_subprocess(
         args.workload, args.cpu_seconds)
+    if cpu is not None:  # context: the oracle over every host core at once
+        cpu["cpu_model"] = cpu_model()
+        cpu["all_cores"] = cpu_baseline_all_cores(args.workload, args.cpu_seconds / 2,
+                                                  min(os.cpu_count() or 1, 16))
     launches = 2 * K  # one write and one decode launch per step
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K,

@@ -74,3 +74,13 @@ def test_reference_arm_prints_its_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["config"]["workload"] == "tiny_int8"
+
+
+def test_oracle_baseline_over_several_cores():
+    """The all-cores oracle baseline runs concurrent single-thread processes and
+    sums their rates; each process's rate is positive, so the sum exceeds none."""
+    r = bench.cpu_baseline_all_cores("tiny_int8", 0.2, 2)
+    assert r is not None and r["cores"] == 2 and r["value"] > 0
+    one = bench.cpu_baseline_subprocess("tiny_int8", 0.2)
+    assert one is not None and one["cores"] == 1 and one["value"] > 0
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
