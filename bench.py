@@ -46,13 +46,16 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   help="the headline workload (timed for exactly --steps steps)")
+    p.add_argument("--workloads", default="all",
+                   help="other workloads measured in the same run: all, none, or a comma list")
     p.add_argument("--ctas", type=int, default=0, help="decode CTAs per kv-head group (0 = auto)")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk-tokens", type=int, default=16384,
-                   help="prefill-chunk write timed when sequence 0 is at least this long (0: off)")
+                   help="prefill-chunk write timed where sequence 0 is at least this long (0: off)")
     p.add_argument("--no-append", action="store_true",
                    help="skip the fused append-and-decode step timing")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -108,30 +111,24 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = {"decode_partition": DECODE_SOURCES, "write_cache": WRITE_SOURCES,
+                  "write_asym": WRITE_ASYM_SOURCES}
+
+
 def profiled_traffic(workload: str, kernel: str = "decode_partition"):
-    """DRAM bytes per launch of a kernel from its committed ncu summary
-    (profiles/<kernel>_<workload>.md), if that was taken on the current
-    sources of the kernel; else None."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    """DRAM bytes per launch of a kernel on a workload, from the machine-readable
+    record of its ncu capture (profiles/<kernel>_<workload>.json), if that
+    capture was taken on the kernel's current sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     if not os.path.exists(path):
         return None
-    vals = {}
-    with open(path) as f:
-        for line in f:
-            if ":" in line and line.strip().startswith("- "):
-                k, v = line.strip()[2:].split(":", 1)
-                vals[k.strip()] = v.strip().strip("`")
-    if kernel == "decode_partition":
-        ok = vals.get("decode_source_sha256_16") == decode_source_hash()
-    elif kernel == "write_asym":
-        ok = vals.get("write_source_sha256_16") == source_hash(WRITE_ASYM_SOURCES)
-    else:
-        ok = vals.get("write_source_sha256_16") == source_hash(WRITE_SOURCES)
-    if not ok:
-        return None
     try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        with open(path) as f:
+            rec = json.load(f)
+        if rec.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel]):
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError, TypeError):
         return None
 
 
@@ -394,212 +391,386 @@ def max_over_ranks(values, device=None):
     return t.tolist()
 
 
-def run_kvq(args, rank: int, world: int, local_rank: int):
+def write_kernel_name(wl) -> str:
+    return "write_asym" if wl.k_fmt.endswith("_asym") else "write_cache"
+
+
+class Case:
+    """One workload resident on the device: inputs, calibrated cache, output,
+    decode workspace and an L2 flush; every call goes through the public API."""
+
+    def __init__(self, name, dev, seed, ctas, l2_bytes):
+        import numpy as np
+        import torch
+        from quantized_paged_kv_kvq_gb300 import kvq
+        from quantized_paged_kv_kvq_gb300 import workloads as W
+        self.kvq, self.dev, self.ctas = kvq, dev, ctas
+        self.wl = wl = W.workload(name, seed=seed, with_data=False)
+        data = W.device_data(wl, dev, seed)
+        self.key, self.value, self.query = data["key"], data["value"], data["query"]
+        self.slots = torch.from_numpy(wl.slot_mapping).to(dev)
+        self.block_table = torch.from_numpy(wl.block_table).to(dev)
+        self.ctx_lens = torch.from_numpy(wl.context_lens).to(dev)
+        self.signs = None if wl.signs is None else torch.from_numpy(wl.signs).to(dev)
+        qmax = {"absmax/127": 127.0, "absmax/448": 448.0}
+
+        def scale(x, rule):  # offline per-tensor calibration (untimed), on the GPU
+            if rule not in qmax:
+                return 1.0
+            o = torch.empty(1, dtype=torch.float32, device=dev)
+            kvq.kvq_calibrate_scale(x.reshape(-1), qmax[rule], o)
+            return float(o.item())
+
+        self.cache = kvq.alloc_kv_cache(wl.k_fmt, wl.v_fmt, wl.num_blocks, wl.block_size,
+                                        wl.num_kv_heads, wl.head_dim,
+                                        scale(self.key, wl.k_scale_rule),
+                                        scale(self.value, wl.v_scale_rule), wl.kvarn,
+                                        self.signs, device=dev)
+        self.out = torch.empty_like(self.query)
+        self.sm_scale = float(np.float32(1.0 / np.sqrt(wl.head_dim)))
+        self.ws_bytes = kvq.kvq_decode_workspace_size(self.cache, wl.num_seqs, wl.num_q_heads,
+                                                      wl.max_context_len, ctas)
+        self.ws = torch.empty(max(self.ws_bytes, 16) // 4 + 4, dtype=torch.float32, device=dev)
+        # L2 flush: write one buffer of 2x L2, then read another of 2x L2, so a
+        # timed kernel starts with an L2 that holds none of its data and no dirty
+        # lines (whose write-back would otherwise land inside the timed kernel)
+        n = max(2 * l2_bytes, 256 << 20)
+        self.flush_w = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.flush_r = torch.ones(n // 4, dtype=torch.int32, device=dev)
+        # each sequence's last token, for the decode step that brings its own token
+        last = np.cumsum(wl.context_lens.astype(np.int64)) - 1
+        self.has_new = wl.context_lens > 0
+        rows = torch.from_numpy(np.where(self.has_new, last, 0)).to(dev)
+        self.new_k = self.key[rows].contiguous()
+        self.new_v = self.value[rows].contiguous()
+        self.last_slots = torch.from_numpy(
+            np.where(self.has_new, wl.slot_mapping[np.where(self.has_new, last, 0)], -1)).to(dev)
+
+    def flush_l2(self):
+        self.flush_w.zero_()
+        self.flush_r.sum()
+
+    def write(self):
+        self.kvq.kvq_write_cache(self.cache, self.key, self.value, self.slots)
+
+    def decode(self):
+        wl = self.wl
+        self.kvq.kvq_paged_decode(self.cache, self.query, self.out, self.block_table,
+                                  self.ctx_lens, wl.max_context_len, self.sm_scale, self.ws,
+                                  self.ctas)
+
+    def append_decode(self, new_k=None, new_v=None, query=None, ctx_lens=None):
+        wl = self.wl
+        self.kvq.kvq_decode_append(self.cache, self.new_k if new_k is None else new_k,
+                                   self.new_v if new_v is None else new_v,
+                                   self.query if query is None else query, self.out,
+                                   self.block_table,
+                                   self.ctx_lens if ctx_lens is None else ctx_lens,
+                                   wl.max_context_len, self.sm_scale, self.ws, self.ctas)
+
+
+def _events(n):
+    import torch
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def time_steps(case, warmup, steps):
+    """`steps` steps of the whole path (flush, write, flush, decode); returns the
+    per-step write and decode times (ms) from CUDA events on the current stream."""
+    import numpy as np
+    import torch
+
+    def step(ev):
+        case.flush_l2()
+        ev[0].record()
+        case.write()
+        ev[1].record()
+        case.flush_l2()
+        ev[2].record()
+        case.decode()
+        ev[3].record()
+
+    for _ in range(warmup):
+        step(_events(4))
+    torch.cuda.synchronize()
+    evs = [_events(4) for _ in range(steps)]
+    for ev in evs:
+        step(ev)
+    torch.cuda.synchronize()
+    w = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    d = np.array([e[2].elapsed_time(e[3]) for e in evs])
+    return w, d
+
+
+def time_write_back_to_back(case, launches):
+    """Cache writes one after another with no flush between them, between one
+    pair of events: a launch's dirty lines are written back during the next
+    ones, so the time per launch includes its DRAM writes (all but the last
+    launch's, 1/launches of them)."""
+    import torch
+    case.flush_l2()
+    e0, e1 = _events(2)
+    e0.record()
+    for _ in range(launches):
+        case.write()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / launches
+
+
+def time_each(case, fn, n, warmup=3):
+    """Median (us) of `fn` over n launches, L2 flushed before each."""
+    import numpy as np
+    import torch
+
+    def one(ev):
+        case.flush_l2()
+        ev[0].record()
+        fn()
+        ev[1].record()
+
+    for _ in range(warmup):
+        one(_events(2))
+    evs = [_events(2) for _ in range(n)]
+    for ev in evs:
+        one(ev)
+    torch.cuda.synchronize()
+    return float(np.median([e[0].elapsed_time(e[1]) for e in evs])) * 1e3
+
+
+def time_append(case, n):
+    """One decode step that brings one new token per sequence: the fused
+    append-and-decode launch, and a cache write of those tokens followed by
+    the decode (both with a flushed L2)."""
+    kvq, wl = case.kvq, case.wl
+    fused = time_each(case, case.append_decode, n)
+    unfused = time_each(case, lambda: (kvq.kvq_write_cache(case.cache, case.new_k, case.new_v,
+                                                           case.last_slots), case.decode()), n)
+    return {"fused_append_decode_us": fused, "write_then_decode_us": unfused, "steps": n,
+            "stat": "median, L2 flushed before each step", "tokens_per_step": int(case.has_new.sum())}
+
+
+def time_chunk(case, tokens, n, seed, hbm):
+    """The write of a `tokens`-token prefill chunk into sequence 0's pages (the
+    long-context shape's prefill step), L2 flushed before each."""
+    import torch
+    from quantized_paged_kv_kvq_gb300 import workloads as W
+    wl = case.wl
+    if tokens <= 0 or int(wl.context_lens[0]) < tokens:
+        return None
+    rows = torch.arange(tokens, device=case.dev)  # sequence 0's first tokens
+    ck, cv = case.key[rows].contiguous(), case.value[rows].contiguous()
+    cs = torch.from_numpy(W.slots_for_context(wl.context_lens[:1] * 0 + tokens,
+                                              wl.block_table[:1], wl.block_size)).to(case.dev)
+    us = time_each(case, lambda: case.kvq.kvq_write_cache(case.cache, ck, cv, cs), n)
+    cbytes = tokens * (2 * wl.num_kv_heads * wl.head_dim * 2 + kv_bytes_per_token(wl) + 8)
+    return {"tokens": tokens, "us": us, "tok_s": tokens / us * 1e6, "gbs": cbytes / us / 1e3,
+            "frac_of_hbm": cbytes / us / 1e3 / hbm, "bytes": cbytes, "steps": n,
+            "stat": "median, L2 flushed before each write"}
+
+
+def e2e_decode_step(case, n, dbytes, world):
+    """A decode step through the public API with host buffers: every step copies
+    its inputs from pinned host memory (the query, each sequence's new key and
+    value row and the context lengths, packed in one buffer: one copy), runs
+    kvq_decode_append (store the new rows, attend over the cache resident in
+    HBM) and copies the output back."""
+    import torch
+    srcs = (case.query, case.new_k, case.new_v, case.ctx_lens)
+    sizes = [x.numel() * x.element_size() for x in srcs]
+    offs, o = [], 0
+    for sz in sizes:  # 16-byte aligned pieces of one packed buffer
+        offs.append(o)
+        o += (sz + 15) // 16 * 16
+    h_buf = torch.empty(o, dtype=torch.uint8).pin_memory()
+    d_buf = torch.empty(o, dtype=torch.uint8, device=case.dev)
+
+    def views(buf):
+        return [buf[a:a + sz].view(x.dtype).view(x.shape) for a, sz, x in zip(offs, sizes, srcs)]
+
+    for h, x in zip(views(h_buf), srcs):
+        h.copy_(x.cpu())
+    d_q, d_k, d_v, d_ctx = views(d_buf)
+    h_out = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+
+    def step():
+        d_buf.copy_(h_buf, non_blocking=True)
+        case.append_decode(new_k=d_k, new_v=d_v, query=d_q, ctx_lens=d_ctx)
+        h_out.copy_(case.out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = _events(2)
+    w0 = time.perf_counter()
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    t = max_over_ranks([e0.elapsed_time(e1) / 1e3], case.dev)[0]
+    return {"value": world * dbytes * n / t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": o,
+            "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": n,
+            "ms_per_step": 1e3 * t / n, "wall_ms_per_step": 1e3 * wall / n,
+            "call": "kvq_decode_append", "tokens_per_step": int(case.has_new.sum())}
+
+
+def e2e_full_context(case, n, dbytes, world):
+    """Write-everything-then-decode through the public API with host buffers:
+    every step copies all bf16 keys and values of the context (and the query,
+    slots, block table, lengths) from pinned host memory, writes the whole
+    cache, decodes and copies the output back -- a prefill-sized step, bound
+    by the host-to-device copy."""
+    import torch
+    srcs = (case.key, case.value, case.query, case.slots, case.block_table, case.ctx_lens)
+    h_in = [x.cpu().pin_memory() for x in srcs]
+    d_in = [torch.empty_like(x) for x in srcs]
+    h_out = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+    kvq, wl = case.kvq, case.wl
+
+    def step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        kvq.kvq_write_cache(case.cache, d_in[0], d_in[1], d_in[3])
+        kvq.kvq_paged_decode(case.cache, d_in[2], case.out, d_in[4], d_in[5], wl.max_context_len,
+                             case.sm_scale, case.ws, case.ctas)
+        h_out.copy_(case.out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = _events(2)
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    t = max_over_ranks([e0.elapsed_time(e1) / 1e3], case.dev)[0]
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    return {"value": world * dbytes * n / t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "steps": n,
+            "ms_per_step": 1e3 * t / n}
+
+
+def roofline(kernel, workload, nbytes, seconds_per_launch, hbm, peak_note):
+    achieved = nbytes / seconds_per_launch / 1e9
+    return {"bound": "hbm", "kernel": kernel + "_kernel", "achieved": achieved, "peak": hbm,
+            "peak_source": peak_note, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": profiled_traffic(workload, kernel), "algorithmic_bytes": nbytes}
+
+
+def measure_case(args, case, rank, world, hbm, peak_note, steps, headline=False):
+    """Time one workload: the whole-path steps (with clocks sampled meanwhile),
+    back-to-back writes, the decode step with its own token and, where the
+    first sequence is long enough, the prefill-chunk write."""
     import numpy as np
     import torch
     import torch.distributed as dist
-
-    from quantized_paged_kv_kvq_gb300 import build as kbuild
-    kbuild.build()
-    from quantized_paged_kv_kvq_gb300 import kvq
-    from quantized_paged_kv_kvq_gb300 import workloads as W
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-
-    wl = W.workload(args.workload, seed=W.SEEDS[args.workload] + 100 * rank)
-    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(torch.bfloat16)
-    key, value, query = bf(wl.key), bf(wl.value), bf(wl.query)
-    slots = torch.from_numpy(wl.slot_mapping).to(dev)
-    block_table = torch.from_numpy(wl.block_table).to(dev)
-    ctx_lens = torch.from_numpy(wl.context_lens).to(dev)
-    signs = None if wl.signs is None else torch.from_numpy(wl.signs).to(dev)
-    qmax = {"absmax/127": 127.0, "absmax/448": 448.0}
-
-    def scale(x, rule):  # offline per-tensor calibration (untimed), on the GPU
-        if rule is None or rule == "1.0":
-            return 1.0
-        o = torch.empty(1, dtype=torch.float32, device=dev)
-        kvq.kvq_calibrate_scale(x.reshape(-1), qmax[rule], o)
-        return float(o.item())
-
-    cache = kvq.alloc_kv_cache(wl.k_fmt, wl.v_fmt, wl.num_blocks, wl.block_size,
-                               wl.num_kv_heads, wl.head_dim, scale(key, wl.k_scale_rule),
-                               scale(value, wl.v_scale_rule), wl.kvarn, signs, device=dev)
-    out = torch.empty_like(query)
-    sm_scale = float(np.float32(1.0 / np.sqrt(wl.head_dim)))
-    P = args.ctas
-    ws_bytes = kvq.kvq_decode_workspace_size(cache, wl.num_seqs, wl.num_q_heads,
-                                             wl.max_context_len, P)
-    ws = torch.empty(max(ws_bytes, 16) // 4 + 4, dtype=torch.float32, device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    # L2 flush: write one buffer of 2x L2, then read another of 2x L2, so the
-    # timed kernels start with an L2 that holds none of their data and no dirty
-    # lines (whose write-back would otherwise land inside the next timed kernel)
-    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
-
-    def flush_l2():
-        flush_w.zero_()
-        flush_r.sum()
-    dargs = (cache, query, out, block_table, ctx_lens, wl.max_context_len, sm_scale, ws, P)
-
-    def step(ev):
-        flush_l2()
-        ev[0].record()
-        kvq.kvq_write_cache(cache, key, value, slots)
-        ev[1].record()
-        flush_l2()
-        ev[2].record()
-        kvq.kvq_paged_decode(*dargs)
-        ev[3].record()
-
-    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    for _ in range(args.warmup):
-        step(mk())
+    wl, dev = case.wl, case.dev
+    for _ in range(args.warmup):  # untimed warm-up steps
+        time_steps(case, 0, 1)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    events = [mk() for _ in range(args.steps)]
-    sampler = ClockSampler(local_rank)
+    sampler = ClockSampler(dev.index or 0)
     sampler.start()
     time.sleep(0.3)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     w0 = time.perf_counter()
-    for ev in events:
-        step(ev)
-    torch.cuda.synchronize()
+    w_ms, d_ms = time_steps(case, 0, steps)
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - w0
     clocks = sampler.stop()
-    w_ms = np.array([e[0].elapsed_time(e[1]) for e in events])
-    d_ms = np.array([e[2].elapsed_time(e[3]) for e in events])
     t_write, t_dec = float(w_ms.sum()) / 1e3, float(d_ms.sum()) / 1e3
-    pct = lambda x: {f"p{q}": round(float(np.percentile(x, q)) * 1e3, 3) for q in (10, 50, 90)}
     t_write, t_dec, wall = max_over_ranks([t_write, t_dec, wall], dev)
     dbytes, wbytes = decode_bytes(wl), write_bytes(wl)
-    K = args.steps
-    gbs = aggregate([t_dec], [world * dbytes * K]) / 1e9
+    pct = lambda x: {f"p{q}": round(float(np.percentile(x, q)) * 1e3, 3) for q in (10, 50, 90)}
+    b2b = max_over_ranks([time_write_back_to_back(case, max(8, min(steps, 50)))], dev)[0]
+    n_side = max(3, min(steps, 200))
+    app = None if args.no_append else time_append(case, n_side)
+    chunk = time_chunk(case, args.chunk_tokens, n_side, W_SEED(wl.name) + 7 + 100 * rank, hbm)
+    r = {
+        "steps": steps,
+        "decode_us": 1e6 * t_dec / steps, "decode_us_pct": pct(d_ms),
+        "decode_gbs": world * dbytes * steps / t_dec / 1e9,
+        "decode_frac_of_hbm": dbytes * steps / t_dec / 1e9 / hbm,
+        "decode_tok_s": world * wl.num_seqs * steps / t_dec,
+        "decode_bytes": dbytes, "decode_split": case.ws_bytes > 0,
+        "cache_write_us": 1e6 * t_write / steps, "cache_write_us_pct": pct(w_ms),
+        "cache_write_gbs": world * wbytes * steps / t_write / 1e9,
+        "cache_write_frac_of_hbm": wbytes * steps / t_write / 1e9 / hbm,
+        "cache_write_tok_s": world * wl.num_tokens * steps / t_write,
+        "write_bytes": wbytes,
+        "cache_write_back_to_back_us": b2b,
+        "cache_write_back_to_back_frac_of_hbm": wbytes / (b2b * 1e-6) / 1e9 / hbm,
+        "roofline_decode": roofline("decode_partition", wl.name, dbytes, t_dec / steps, hbm,
+                                    peak_note),
+        "roofline_write": roofline(write_kernel_name(wl), wl.name, wbytes, t_write / steps, hbm,
+                                   peak_note),
+        "decode_step_append": app,
+        "prefill_chunk_write": chunk,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+        "shape": {"num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+                  "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                  "block_size": wl.block_size, "k_fmt": wl.k_fmt, "v_fmt": wl.v_fmt,
+                  "kvarn": wl.kvarn, "context_tokens": int(wl.context_lens.sum())},
+    }
+    return r, t_write, t_dec
+
+
+def W_SEED(name):
+    from quantized_paged_kv_kvq_gb300 import workloads as W
+    return W.SEEDS[name]
+
+
+def run_kvq(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_paged_kv_kvq_gb300 import build as kbuild
+    kbuild.build()
+    from quantized_paged_kv_kvq_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     hbm, peak_src = measured_peaks()
-    achieved = dbytes / (t_dec / K) / 1e9
-    achieved_w = wbytes / (t_write / K) / 1e9
     peak_note = f"{peak_src} hbm_gbs (burst copy)"
-    rl_decode = {"bound": "hbm", "kernel": "decode_partition_kernel", "achieved": achieved,
-                 "peak": hbm, "peak_source": peak_note, "unit": "GB/s", "frac": achieved / hbm,
-                 "traffic": profiled_traffic(args.workload, "decode_partition"),
-                 "algorithmic_bytes": dbytes}
-    wkern = "write_asym" if wl.k_fmt.endswith("_asym") else "write_cache"
-    rl_write = {"bound": "hbm", "kernel": wkern + "_kernel", "achieved": achieved_w,
-                "peak": hbm, "peak_source": peak_note, "unit": "GB/s", "frac": achieved_w / hbm,
-                "traffic": profiled_traffic(args.workload, wkern),
-                "algorithmic_bytes": wbytes}
+    K = args.steps
 
-    # one decode step that brings its own token (one per sequence): the fused
-    # append-and-decode launch against a cache write of those tokens followed by
-    # the decode (both with a flushed L2; outside the timed region above)
-    step_lat = None
-    if not args.no_append:
-        last = np.cumsum(wl.context_lens.astype(np.int64)) - 1
-        has = wl.context_lens > 0
-        rows = torch.from_numpy(np.where(has, last, 0)).to(dev)
-        new_k, new_v = key[rows].contiguous(), value[rows].contiguous()
-        last_slots = torch.from_numpy(np.where(has, wl.slot_mapping[np.where(has, last, 0)],
-                                               -1)).to(dev)
-        n_app = max(3, min(K, 200))
-
-        def fused(ev):
-            flush_l2()
-            ev[0].record()
-            kvq.kvq_decode_append(cache, new_k, new_v, query, out, block_table, ctx_lens,
-                                  wl.max_context_len, sm_scale, ws, P)
-            ev[1].record()
-
-        def unfused(ev):
-            flush_l2()
-            ev[0].record()
-            kvq.kvq_write_cache(cache, new_k, new_v, last_slots)
-            kvq.kvq_paged_decode(*dargs)
-            ev[1].record()
-
-        res = {}
-        for name, fn in (("fused", fused), ("unfused", unfused)):
-            for _ in range(3):
-                fn(mk())
-            evs = [mk() for _ in range(n_app)]
-            for ev in evs:
-                fn(ev)
-            torch.cuda.synchronize()
-            ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
-            res[name] = max_over_ranks([float(np.median(ms)) * 1e3], dev)[0]
-        step_lat = {"fused_append_decode_us": res["fused"],
-                    "write_then_decode_us": res["unfused"], "steps": n_app,
-                    "stat": "median, L2 flushed before each step", "tokens_per_step": int(has.sum())}
-
-    # a prefill chunk: the write of `chunk_tokens` new tokens into sequence 0's
-    # pages (the long-context shape's prefill step), L2 flushed before each
-    chunk = None
-    C = args.chunk_tokens
-    if C > 0 and int(wl.context_lens[0]) >= C:
-        pc = W.prefill_chunk(wl, C, seed=W.SEEDS[args.workload] + 7 + 100 * rank)
-        ck, cv = bf(pc["key"]), bf(pc["value"])
-        cs = torch.from_numpy(pc["slot_mapping"]).to(dev)
-        n_ch = max(3, min(K, 200))
-
-        def chunk_write(ev):
-            flush_l2()
-            ev[0].record()
-            kvq.kvq_write_cache(cache, ck, cv, cs)
-            ev[1].record()
-
-        for _ in range(3):
-            chunk_write(mk())
-        evs = [mk() for _ in range(n_ch)]
-        for ev in evs:
-            chunk_write(ev)
-        torch.cuda.synchronize()
-        us = max_over_ranks([float(np.median([e[0].elapsed_time(e[1]) for e in evs])) * 1e3],
-                            dev)[0]
-        cbytes = C * (2 * wl.num_kv_heads * wl.head_dim * 2 + kv_bytes_per_token(wl) + 8)
-        chunk = {"tokens": C, "us": us, "tok_s": C / us * 1e6, "gbs": cbytes / us / 1e3,
-                 "frac_of_hbm": cbytes / us / 1e3 / hbm, "steps": n_ch,
-                 "stat": "median, L2 flushed before each write"}
-
-    # end to end through the public API: pinned host inputs in, result out
-    e2e = None
+    # ---- the headline workload: exactly K timed steps, then the side legs
+    case = Case(args.workload, dev, W.SEEDS[args.workload] + 100 * rank, args.ctas, l2)
+    head, t_write, t_dec = measure_case(args, case, rank, world, hbm, peak_note, K, headline=True)
+    wl = case.wl
+    dbytes = decode_bytes(wl)
+    e2e = e2e_full = None
     if not args.no_e2e:
-        pin = lambda t: t.cpu().pin_memory()
-        h_in = [pin(x) for x in (key, value, query, slots, block_table, ctx_lens)]
-        d_in = [torch.empty_like(x) for x in (key, value, query, slots, block_table, ctx_lens)]
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         n_e2e = max(1, min(args.e2e_steps, K))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e = e2e_decode_step(case, max(n_e2e, 20), dbytes, world)
+        e2e_full = e2e_full_context(case, n_e2e, dbytes, world)
+    ws_desc = case.ws_bytes
+    del case
+    torch.cuda.empty_cache()
 
-        def e2e_step():
-            for h, d in zip(h_in, d_in):
-                d.copy_(h, non_blocking=True)
-            kvq.kvq_write_cache(cache, d_in[0], d_in[1], d_in[3])
-            kvq.kvq_paged_decode(cache, d_in[2], out, d_in[4], d_in[5], wl.max_context_len,
-                                 sm_scale, ws, P)
-            h_out.copy_(out, non_blocking=True)
-
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0.record()
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record()
-        torch.cuda.synchronize()
-        t_e2e = max_over_ranks([e0.elapsed_time(e1) / 1e3], dev)[0]
-        h2d = sum(x.numel() * x.element_size() for x in h_in)
-        e2e = {"value": world * dbytes * n_e2e / t_e2e / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h_out.numel() * 2,
-               "steps": n_e2e, "ms_per_step": 1e3 * t_e2e / n_e2e}
+    # ---- every other configuration, each with its own clocks
+    names = [] if args.workloads == "none" else (
+        list(W.WORKLOADS) if args.workloads == "all" else args.workloads.split(","))
+    per = {args.workload: head}
+    n_cfg = min(max(K, 50), 500)
+    for name in names:
+        if name in per:
+            continue
+        c = Case(name, dev, W.SEEDS[name] + 100 * rank, args.ctas, l2)
+        per[name], _, _ = measure_case(args, c, rank, world, hbm, peak_note, n_cfg)
+        del c
+        torch.cuda.empty_cache()
 
     if world > 1:
         dist.barrier()
@@ -612,10 +783,10 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
         cpu["cpu_model"] = cpu_model()
         cpu["all_cores"] = cpu_baseline_all_cores(args.workload, args.cpu_seconds / 2,
                                                   min(os.cpu_count() or 1, 16))
-    launches = 2 * K  # one write and one decode launch per step
+    rl_d, rl_w = head["roofline_decode"], head["roofline_write"]
     line = {
-        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": 1e3 * (t_write + t_dec) / K,
+        "metric": METRIC, "value": head["decode_gbs"], "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * (t_write + t_dec) / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic",
         "config": {"workload": args.workload, "num_seqs": wl.num_seqs,
@@ -623,28 +794,34 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
                    "head_dim": wl.head_dim, "block_size": wl.block_size,
                    "k_fmt": wl.k_fmt, "v_fmt": wl.v_fmt, "kvarn": wl.kvarn,
                    "context_tokens": int(wl.context_lens.sum()),
-                   "decode_ctas": P or "auto", "l2": "flushed before the write and before the decode (2xL2 memset, "
-                   "then a 2xL2 read), outside the timed events"},
-        "decode_tok_s": world * wl.num_seqs * K / t_dec,
-        "decode_us": 1e6 * t_dec / K, "decode_us_pct": pct(d_ms),
-        "decode_split": ws_bytes > 0,
-        "cache_write_tok_s": world * wl.num_tokens * K / t_write,
-        "cache_write_gbs": world * wbytes * K / t_write / 1e9,
-        "cache_write_us": 1e6 * t_write / K, "cache_write_us_pct": pct(w_ms),
-        "cache_write_frac_of_hbm": (wbytes * K / t_write / 1e9) / hbm,
-        "decode_bytes": dbytes, "write_bytes": wbytes,
-        "wall_s_timed_region": wall,
+                   "decode_ctas": args.ctas or "auto",
+                   "l2": "flushed before the write and before the decode (2xL2 memset, "
+                         "then a 2xL2 read), outside the timed events",
+                   "inputs": "drawn on the device (torch generator) by the workload recipe"},
+        "decode_tok_s": head["decode_tok_s"], "decode_us": head["decode_us"],
+        "decode_us_pct": head["decode_us_pct"], "decode_split": ws_desc > 0,
+        "cache_write_tok_s": head["cache_write_tok_s"],
+        "cache_write_gbs": head["cache_write_gbs"], "cache_write_us": head["cache_write_us"],
+        "cache_write_us_pct": head["cache_write_us_pct"],
+        "cache_write_frac_of_hbm": head["cache_write_frac_of_hbm"],
+        "cache_write_back_to_back_us": head["cache_write_back_to_back_us"],
+        "cache_write_back_to_back_frac_of_hbm": head["cache_write_back_to_back_frac_of_hbm"],
+        "decode_bytes": head["decode_bytes"], "write_bytes": head["write_bytes"],
+        "wall_s_timed_region": head["wall_s_timed_region"],
         # the dominant kernel of the step (largest share of its time) first
-        "roofline": rl_write if t_write >= t_dec else rl_decode,
-        "roofline_decode": rl_decode,
-        "roofline_write": rl_write,
-        "decode_frac_of_hbm": gbs / world / hbm,
+        "roofline": rl_w if t_write >= t_dec else rl_d,
+        "roofline_decode": rl_d,
+        "roofline_write": rl_w,
+        "decode_frac_of_hbm": head["decode_frac_of_hbm"],
         "e2e": e2e,
-        "decode_step_append": step_lat,
-        "prefill_chunk_write": chunk,
-        "gpu_launches": launches,
-        "clocks": clocks,
+        "e2e_full_context": e2e_full,
+        "decode_step_append": head["decode_step_append"],
+        # the long-context configuration's prefill chunk (where the run measured it)
+        "prefill_chunk_write": (per.get("kvarn_131k") or {}).get("prefill_chunk_write"),
+        "gpu_launches": 2 * K,  # one write and one decode launch per timed step
+        "clocks": head["clocks"],
         "cpu_baseline": cpu,
+        "workloads": {k: {kk: vv for kk, vv in v.items()} for k, v in per.items()},
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -258,7 +258,10 @@ kvq_status kvq_decode_append(const kvq_cache_desc* cache, void* k_cache, void* v
  *
  * The first call on a device looks up the scratch's device address (once per
  * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array, and it keeps whatever the last
+ * capture.  The address is kept with the id of the context it belongs to, so
+ * a call after cudaDeviceReset (a new primary context) looks it up again.
+ * `stream` must belong to the current device: the scratch used is the current
+ * device's copy.  All calls share the one array, and it keeps whatever the last
  * call left: nothing in it needs to start at zero (every value the combine
  * reads is written earlier in the same call), but two calls whose kernels
  * overlap on the GPU (different streams, or several host threads) race on it

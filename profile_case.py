@@ -3,24 +3,27 @@
 A small, fixed case for a profiler to capture (the bench's full-size workloads are
 too large for a multi-pass capture):
 
-  python -m quantized_paged_kv_kvq_gb300.profile_case kvarn_131k num_seqs=1 \
-      ctx_lo=32768 ctx_hi=32768
+  python profile_case.py kvarn_131k num_seqs=1 ctx_lo=32768 ctx_hi=32768
 
 Arguments after the workload name override its generator settings (integers).
 Everything goes through the library's public calls; nothing is checked here.
 """
 from __future__ import annotations
 
+import os
 import sys
 
 import numpy as np
 import torch
 
-from . import kvq
-from . import workloads as W
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from quantized_paged_kv_kvq_gb300 import build as kbuild  # noqa: E402
+from quantized_paged_kv_kvq_gb300 import kvq  # noqa: E402
+from quantized_paged_kv_kvq_gb300 import workloads as W  # noqa: E402
 
 
 def run(name: str, repeats: int = 3, **overrides) -> None:
+    kbuild.build()
     wl = W.workload(name, **overrides)
     dev = torch.device("cuda", 0)
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(torch.bfloat16)

@@ -438,122 +438,6 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
-// Log-sum-exp merge of the partial results of sequence s (tiles [ps, ps+tiles)
-// of the global order) held in the slots of stream-K ranges ka..kb, by one warp
-// for its kv-head's G query heads, four at a time.  A slot holds, per query
-// head, the range's normalised output acc/l in fp16 and (m, l) in fp32, and
-// out = sum_i 2^(m_i - M) l_i (acc_i / l_i) / sum_i 2^(m_i - M) l_i.  Lane
-// (nn, r) owns query head nn's dims 64i + 8r + e (i < DL/8, e < 8), so each
-// 16-byte load instruction of the warp reads whole 128-byte lines.  Every lane
-// reads every range's (m, l) itself; the loads of PU ranges are issued
-// together and merged with a running maximum: a few L2 round trips per merge.
-template <int D, bool KVARN>
-__device__ __forceinline__ void merge_partials(const DecodeArgs& a, int s, long long ps, int tiles,
-                                               long long T, int NC, int HG, int hg, int warp,
-                                               int lane, int hpc) {
-  constexpr int LQ = 8;                     // lanes per query head
-  constexpr int DL = D / LQ;                // dims per lane
-  constexpr int PU = 4;        // ranges per batch of loads
-  const int G = a.gqa, rows = hpc * G;
-  const int r = lane % LQ;
-  const int ka = range_of(a, ps, T), kb = range_of(a, ps + tiles - 1, T);
-  const int np = kb - ka + 1;
-  const int h = hg * hpc + warp;
-#pragma unroll 1
-  for (int n0 = 0; n0 < G; n0 += 32 / LQ) {  // every lane runs every pass (shuffles below)
-    const int nn = n0 + lane / LQ;
-    const bool act = nn < G;
-    float M = -INFINITY, Lsum = 0.f;
-    float acc[DL];
-#pragma unroll
-    for (int e = 0; e < DL; ++e) acc[e] = 0.f;
-#pragma unroll 1
-    for (int c0 = 0; c0 < np; c0 += 32) {  // ranges ka+c0 .. ka+c0+31
-      // lane p: first slot row of range ka + c0 + p, or -1 if that range is empty
-      int base = -1;
-      if (c0 + lane < np) {
-        const int kk = ka + c0 + lane;
-        const long long r0 = range_start(a, T, kk), r1 = range_start(a, T, kk + 1);
-        if (r0 < r1) base = ((kk * HG + hg) * 2 + (r0 >= ps ? 0 : 1)) * rows;
-      }
-      const int cn = min(32, np - c0);
-#pragma unroll 1
-      for (int p0 = 0; p0 < cn; p0 += PU) {
-        float ml[PU][2];
-        uint4 v[PU][DL / 8];
-#pragma unroll
-        for (int u = 0; u < PU; ++u) {
-          const int b = __shfl_sync(0xffffffffu, base, (p0 + u) & 31);
-          if (act && p0 + u < cn && b >= 0) {
-            const long long sl = static_cast<long long>(b) + warp * G + nn;
-            const float2 x = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + 2 * sl));
-            ml[u][0] = x.x;
-            ml[u][1] = x.y;
-            ldcg_halves<DL>(a.ws_acc + sl * D + 8 * r, v[u]);
-          } else {
-            ml[u][0] = -INFINITY;
-            ml[u][1] = 0.f;
-#pragma unroll
-            for (int i = 0; i < DL / 8; ++i) v[u][i] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        float bm = ml[0][0];
-#pragma unroll
-        for (int u = 1; u < PU; ++u) bm = fmaxf(bm, ml[u][0]);
-        // no slot in this batch (empty ranges; more ranges than tiles): nothing to
-        // add, and 2^(m - M) would be 2^(-inf + inf) while M is still -inf
-        if (bm == -INFINITY) continue;
-        if (bm > M) {  // raise the running maximum, rescaling what was summed so far
-          const float sc = fast_exp2(M - bm);
-          Lsum *= sc;
-#pragma unroll
-          for (int e = 0; e < DL; ++e) acc[e] *= sc;
-          M = bm;
-        }
-#pragma unroll
-        for (int u = 0; u < PU; ++u) {
-          const float w = fast_exp2(ml[u][0] - M) * ml[u][1];  // 2^(m - M) l
-          Lsum += w;
-#pragma unroll
-          for (int i = 0; i < DL / 8; ++i) {
-            const uint32_t q[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float2 f = half2_bits_to_float2(q[t]);
-              acc[8 * i + 2 * t] += w * f.x;
-              acc[8 * i + 2 * t + 1] += w * f.y;
-            }
-          }
-        }
-      }
-    }
-    const float il = act ? 1.0f / Lsum : 0.f;
-#pragma unroll
-    for (int e = 0; e < DL; ++e) acc[e] *= il;
-    if constexpr (KVARN) {  // inverse rotation x = d . (cR * H y): the Walsh-Hadamard
-      // matrix is unchanged by a permutation of index bits, so the butterflies run
-      // over the local index (dim bits 0-2, 6) and then across the lanes (3-5)
-      fwht_lanes<DL, LQ>(acc, r);
-#pragma unroll
-      for (int e = 0; e < DL; ++e) {
-        const int dd = 64 * (e >> 3) + 8 * r + (e & 7);
-        const float sgn = (a.signs != nullptr && a.signs[dd] < 0) ? -1.f : 1.f;
-        acc[e] = __fmul_rn(acc[e], a.cR) * sgn;
-      }
-    }
-    if (act) {
-      uint16_t* orow = a.out + (static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G + nn) * D + 8 * r;
-#pragma unroll
-      for (int i = 0; i < DL / 8; ++i) {
-        float piece[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) piece[e] = acc[8 * i + e];
-        store_bf16_run<8>(orow + 64 * i, piece);
-      }
-    }
-  }
-}
-
 constexpr int kTeam = 8;       // ranges merged together at the first level of a tree
 constexpr int kTreeRanges = 32;  // sequences over more ranges than this merge in two levels
 
@@ -1441,8 +1325,8 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     const int s = static_cast<int>(info >> 32), tiles = static_cast<int>(info & 0xFFFFFFFFll);
     const long long ps = scratch[12 + 2 * pm];
     const int ka = range_of(a, ps, Tm), kb = range_of(a, ps + tiles - 1, Tm);
-    if (kb - ka + 1 <= kTreeRanges) {
-      merge_partials<D, KVARN>(a, s, ps, tiles, Tm, NC, HG, hg, warp, lane, hpc);
+    if (kb - ka + 1 <= kTreeRanges) {  // one level: every range's slot, straight to the output
+      merge_slots<D, KVARN>(a, s, ps, Tm, HG, hg, warp, lane, hpc, ka, 1, kb - ka + 1, kb, -1);
       continue;
     }
     const int nteams = (kb - ka) / kTeam + 1;

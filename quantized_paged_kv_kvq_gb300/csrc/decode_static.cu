@@ -7,8 +7,14 @@
 // that loads the library holds that much for the life of the process.
 // Host code may not use the array's name as a device address (on the host it
 // names a stand-in object), so its device address is looked up with
-// cudaGetSymbolAddress once per device, with that device current, on the
-// first call made on the device, and cached.
+// cudaGetSymbolAddress, with the device current, on the first call made on
+// the device, and cached together with the unique id of the context it was
+// looked up in: a call made in another context of that device (after a
+// cudaDeviceReset, the library's module is loaded again, possibly elsewhere)
+// looks it up again.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "../../include/kvq.h"
@@ -23,17 +29,45 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBy
 
 std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_decode_scratch on the current device (looked up once).
+// Unique id of the calling thread's current context (0 if it cannot be read).
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_decode_scratch on the current device (looked up once per
+// device and context).
 kvq_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  if (g_scratch_ptr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
       return KVQ_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = current_context_id();  // the lookup made the context current
   }
   *out = g_scratch_ptr[dev];
   return KVQ_OK;

@@ -149,6 +149,7 @@ def make_workload(
     token_magnitude_sigma: float = 0.0,
     spare_blocks: int = 4,
     context_lens: Optional[np.ndarray] = None,
+    with_data: bool = True,
 ) -> Workload:
     # two independent streams: the paged layout (lengths, block permutation) and
     # the tensor data, so that changing the block size keeps the same K/V/q
@@ -160,6 +161,19 @@ def make_workload(
     table, nb = _paged_layout(rng, context_lens, block_size, spare_blocks)
     slots = slots_for_context(context_lens, table, block_size)
     t = int(slots.shape[0])
+    recipe = dict(k_outliers=tuple(k_outliers), token_magnitude_sigma=token_magnitude_sigma)
+    if not with_data:  # the paged layout only; tensors come from device_data()
+        signs = None
+        if kvarn:
+            srng = np.random.Generator(np.random.PCG64([seed, 2]))
+            signs = np.where(srng.integers(0, 2, size=head_dim) == 0, 1, -1).astype(np.int8)
+        return Workload(
+            name=name, seed=seed, num_seqs=num_seqs, num_q_heads=num_q_heads,
+            num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=block_size,
+            k_fmt=k_fmt, v_fmt=v_fmt, kvarn=kvarn, k_scale_rule=k_scale_rule,
+            v_scale_rule=v_scale_rule, context_lens=context_lens, block_table=table,
+            num_blocks=nb, slot_mapping=slots, key=None, value=None, query=None, signs=signs,
+            extra=recipe)
     rng = np.random.Generator(np.random.PCG64([seed, 1]))
     key = _normal(rng, (t, num_kv_heads, head_dim))
     if k_outliers[0]:
@@ -180,7 +194,7 @@ def make_workload(
         k_fmt=k_fmt, v_fmt=v_fmt, kvarn=kvarn, k_scale_rule=k_scale_rule,
         v_scale_rule=v_scale_rule, context_lens=context_lens, block_table=table,
         num_blocks=nb, slot_mapping=slots, key=round_to_bf16(key),
-        value=round_to_bf16(value), query=round_to_bf16(query), signs=signs,
+        value=round_to_bf16(value), query=round_to_bf16(query), signs=signs, extra=recipe,
     )
 
 
@@ -227,6 +241,39 @@ def workload(name: str, **overrides) -> Workload:
     kw.update(overrides)
     seed = kw.pop("seed", SEEDS[name])
     return make_workload(name=name, seed=seed, **kw)
+
+
+def device_data(wl: Workload, device, seed: Optional[int] = None) -> dict:
+    """The tensors of a layout-only workload (with_data=False), drawn on the
+    device with torch's generator by the same recipe as make_workload: normal
+    q, K, V; the seeded outlier channels of K; KVarN's per-row magnitudes of
+    K; every value rounded to bfloat16 (nearest, ties to even).  The values
+    differ from the numpy stream (another generator) but follow the same
+    distributions; used where only sizes and statistics matter (timing).
+    Returns bf16 tensors key, value [T, Hkv, D] and query [S, Hq, D]."""
+    import torch
+    seed = wl.seed if seed is None else seed
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    t, hkv, d = wl.num_tokens, wl.num_kv_heads, wl.head_dim
+    rng = np.random.Generator(np.random.PCG64([seed, 3]))
+
+    def normal(shape):
+        return torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+
+    key = normal((t, hkv, d))
+    n_out, factor = wl.extra.get("k_outliers", (0, 1.0))
+    if n_out:
+        for h in range(hkv):
+            ch = torch.from_numpy(rng.choice(d, size=n_out, replace=False)).to(device)
+            key[:, h, ch] *= float(factor)
+    sigma = wl.extra.get("token_magnitude_sigma", 0.0)
+    if sigma:
+        key *= torch.exp(torch.randn((t, hkv, 1), generator=g, device=device) * sigma)
+    value = normal((t, hkv, d))
+    query = normal((wl.num_seqs, wl.num_q_heads, d))
+    return dict(key=key.to(torch.bfloat16), value=value.to(torch.bfloat16),
+                query=query.to(torch.bfloat16))
 
 
 def prefill_chunk(wl: Workload, num_tokens: int, seed: int) -> dict:

@@ -8,6 +8,7 @@ import socket
 import sys
 from contextlib import redirect_stdout
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -84,3 +85,50 @@ def test_oracle_baseline_over_several_cores():
     one = bench.cpu_baseline_subprocess("tiny_int8", 0.2)
     assert one is not None and one["cores"] == 1 and one["value"] > 0
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_profiled_traffic_reads_json_sidecars(tmp_path, monkeypatch):
+    """A sidecar counts only while its source hash is that of the kernel's
+    current sources; a missing or malformed one gives None."""
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    assert bench.profiled_traffic("w", "decode_partition") is None
+    monkeypatch.setattr(bench, "ROOT", ROOT)
+    good = bench.source_hash(bench.DECODE_SOURCES)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda names: good)
+    rec = {"kernel": "decode_partition", "workload": "w", "source_sha256_16": good,
+           "dram_bytes_per_launch": 12345}
+    (tmp_path / "profiles" / "decode_partition_w.json").write_text(json.dumps(rec))
+    assert bench.profiled_traffic("w", "decode_partition") == 12345.0
+    rec["source_sha256_16"] = "0" * 16
+    (tmp_path / "profiles" / "decode_partition_w.json").write_text(json.dumps(rec))
+    assert bench.profiled_traffic("w", "decode_partition") is None
+    (tmp_path / "profiles" / "decode_partition_w.json").write_text("{not json")
+    assert bench.profiled_traffic("w", "decode_partition") is None
+
+
+def test_committed_sidecars_name_their_kernel_and_workload():
+    import glob
+    from quantized_paged_kv_kvq_gb300 import workloads as W
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.json")):
+        rec = json.load(open(path))
+        assert rec["kernel"] in bench.KERNEL_SOURCES and rec["workload"] in W.WORKLOADS
+        assert os.path.basename(path) == f"{rec['kernel']}_{rec['workload']}.json"
+        assert int(rec["dram_bytes_per_launch"]) > 0
+
+
+def test_layout_only_workload_has_the_same_layout():
+    """The bench draws its tensors on the device but takes the paged layout
+    (lengths, block table, slots) from the same seeded generator."""
+    from quantized_paged_kv_kvq_gb300 import workloads as W
+    for name, kw in (("llama8b_int8", dict(num_seqs=5, ctx_lo=10, ctx_hi=300)),
+                     ("kvarn_131k", dict(num_seqs=2, ctx_lo=33, ctx_hi=70))):
+        a = W.workload(name, **kw)
+        b = W.workload(name, with_data=False, **kw)
+        assert b.key is None and b.value is None and b.query is None
+        for f in ("context_lens", "block_table", "slot_mapping"):
+            assert np.array_equal(getattr(a, f), getattr(b, f))
+        assert a.num_blocks == b.num_blocks and a.extra == b.extra
+        if a.kvarn:
+            assert b.signs is not None and set(np.unique(b.signs)) <= {-1, 1}

@@ -64,6 +64,59 @@ def test_hadamard_rows_bf16_output_is_rounded_f32_result():
     assert np.all(np.abs(y16 - y32) <= np.abs(y32) * 2.0 ** -8)
 
 
+def _bf16(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32)
+
+
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_hadamard_rows_bf16_rounds_ties_to_even(sign):
+    """D = 64, so cR = 1/8 exactly and a row a*e0 + b*e1 rotates to (a + b)/8
+    and (a - b)/8 (alternating positions) with no rounding before the bf16
+    store; b = 2^-8 puts these on or off bf16 ties:
+      a = 1:          a + b = 1 + 2^-8, halfway between 1 (even) and 1 + 2^-7:
+                      ties-to-even gives 1, ties-away or rounding up 1 + 2^-7;
+                      a - b = 1 - 2^-8 is a bf16 value (no rounding).
+      a = 1 + 2^-7:   a + b = 1 + 3*2^-8, halfway between 1 + 2^-7 (odd) and
+                      1 + 2^-6 (even): ties-to-even rounds up, ties-to-odd or
+                      truncation stay at 1 + 2^-7;
+                      a - b = 1 + 2^-8, a tie again: ties-to-even gives 1."""
+    d = 64
+    cases = ((1.0, 1.0, 1.0 + 2.0 ** -7, 1.0 - 2.0 ** -8),
+             (1.0 + 2.0 ** -7, 1.0 + 2.0 ** -6, 1.0 + 2.0 ** -7, 1.0))
+    b = 2.0 ** -8
+    for a, plus_even, plus_wrong, minus_even in cases:
+        x = np.zeros((1, d), np.float32)
+        x[0, 0], x[0, 1] = sign * a, sign * b
+        y32 = H.hadamard_rows(x, None, False, "f32")
+        y16 = H.hadamard_rows(x, None, False, "bf16")
+        assert np.all(y32[0, 0::2] == np.float32(sign * (a + b) / 8))  # exact in float32
+        assert np.all(y32[0, 1::2] == np.float32(sign * (a - b) / 8))
+        assert np.all(y16[0, 0::2] == np.float32(sign * plus_even / 8))
+        assert np.all(y16[0, 0::2] != np.float32(sign * plus_wrong / 8))
+        assert np.all(y16[0, 1::2] == np.float32(sign * minus_even / 8))
+
+
+def test_hadamard_rows_bf16_rounding_matches_torch():
+    """Random rows, and rows whose float32 result sits exactly on bf16 ties:
+    the bf16 store equals torch's float32 -> bfloat16 conversion (round to
+    nearest, ties to even)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(21)
+    x = _bf16(rng.integers(0x3000, 0x4300, size=(64, 64)) | (rng.integers(0, 2, (64, 64)) << 15))
+    x[:32] = 0
+    # rows a e0 + b e1 with (a + b) on a tie: a any bf16, b = half an ulp of a
+    a = _bf16(rng.integers(0x3E00, 0x4100, size=32) | (rng.integers(0, 2, 32) << 15))
+    ulp_half = (a.view(np.uint32) & 0x7F800000).view(np.float32) * np.float32(2.0 ** -8)
+    x[:32, 0], x[:32, 1] = a, ulp_half * np.sign(a)
+    for inverse in (False, True):
+        y32 = H.hadamard_rows(x, None, inverse, "f32")
+        y16 = H.hadamard_rows(x, None, inverse, "bf16")
+        ref = torch.from_numpy(y32).to(torch.bfloat16).to(torch.float32).numpy()
+        assert np.array_equal(y16.view(np.uint32), ref.view(np.uint32))
+    ties = (H.hadamard_rows(x[:32], None, False, "f32").view(np.uint32) & 0xFFFF) == 0x8000
+    assert ties.sum() >= 32 * 16  # the tie rows really do land on ties
+
+
 def test_tree_sum_order_is_pinned():
     """Group sums go left to right; groups combine largest offset first."""
     d = 128

@@ -11,7 +11,7 @@ import torch
 from quantized_paged_kv_kvq_gb300 import kvq
 from quantized_paged_kv_kvq_gb300 import workloads as W
 
-from kvq_testing import GpuRun, assert_attention_close, out_numpy
+from kvq_testing import GpuRun, OracleRun, assert_attention_close, out_numpy
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +40,25 @@ def test_static_scratch_decode_matches_workspace_decode_twice():
         got = out_numpy(_static_decode(g, ctas))
         assert np.all(np.isfinite(got))
         assert_attention_close(got, ref, f"static vs workspace, {wl.name}")
+    assert kvq.kvq_get_device_error() == 0
+
+
+@pytest.mark.parametrize("ctas", [64, 0])
+def test_static_scratch_long_sequence_against_oracle(ctas):
+    """One long KVarN sequence over 64 ranges (more than 32: merged in two
+    levels, whose team tags and claims sit deeper in the scratch) and over the
+    automatic grid (a size that depends on the SM count), after the calls
+    above have left their own contents in the scratch."""
+    lens = np.array([8192], np.int32)
+    wl = W.workload("kvarn_131k", num_seqs=1, context_lens=lens)
+    g = GpuRun(wl)
+    g.write()
+    need = kvq.kvq_decode_workspace_size(g.cache, wl.num_seqs, wl.num_q_heads,
+                                         wl.max_context_len, ctas)
+    assert 0 < need <= kvq.kvq_paged_decode_static_capacity()
+    got = out_numpy(_static_decode(g, ctas))
+    assert np.all(np.isfinite(got))
+    assert_attention_close(got, OracleRun(wl).decode(), f"static, kvarn 8192 tokens, ctas={ctas}")
     assert kvq.kvq_get_device_error() == 0
 
 
