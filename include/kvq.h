@@ -319,7 +319,22 @@ kvq_status kvq_calibrate_head_scales(const void* x, int64_t num_tokens, int32_t 
 #define KVQ_DEVERR_BLOCK_RANGE 2u /* a block-table entry outside [0, num_blocks) */
 #define KVQ_DEVERR_CONTEXT_RANGE 4u /* a context length outside [0, max_context_len] */
 #define KVQ_DEVERR_COMBINE 8u       /* a split-sequence merge counter update gave up */
-#define KVQ_DEVERR_TIMEOUT 16u      /* a pipeline barrier wait gave up (results invalid) */
+#define KVQ_DEVERR_TIMEOUT 16u      /* a pipeline barrier wait gave up: the CTA stopped
+                                       early, the launch's results are invalid */
+
+/*
+ * kvq_debug_arm_wait_timeout -- test hook for the decode kernel's bounded
+ * pipeline waits (every mbarrier wait gives up after a number of polls, sets
+ * KVQ_DEVERR_TIMEOUT and makes its CTA stop loading, publish nothing and
+ * return once no copy it issued is in flight).  It applies to the next decode
+ * launch of the process (kvq_paged_decode*, kvq_decode_append) and then
+ * disarms itself: that launch polls each wait at most `polls` times (>= 1),
+ * and CTA `cta` of the first kv-head group never issues the loads of the
+ * `tile`-th tile of its range (-1: every load is issued), so that the waits
+ * for that tile run out with nothing in flight.  The launch's output is then
+ * invalid.  For tests of the failure path only; a caller never needs it.
+ */
+kvq_status kvq_debug_arm_wait_timeout(int32_t polls, int32_t cta, int32_t tile);
 
 /*
  * kvq_get_device_error -- synchronizes `stream`, then reads and clears the

@@ -100,6 +100,16 @@ size_t workspace_bytes_for(int num_seqs, int hq, int hkv, int d, int nc) {
          static_cast<size_t>(num_seqs) * groups * 8;
 }
 
+// Test hook of the bounded pipeline waits (kvq_debug_arm_wait_timeout): armed
+// for the next decode launch of the process only.
+std::atomic<int> g_wait_hook_armed{0};
+std::atomic<int> g_wait_hook_polls{0};
+std::atomic<int> g_wait_hook_cta{-1};
+std::atomic<int> g_wait_hook_tile{-1};
+
+// Polls of an mbarrier before a decode CTA gives up (the kernel's default).
+constexpr int kDefaultSpinLimit = 1 << 22;
+
 // Nonzero 64-bit tag, different for every decode call of the process, so that
 // the completion tags never need clearing between calls.
 unsigned long long next_epoch() {
@@ -299,6 +309,14 @@ kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const v
   volatile float one = 1.0f;  // 1/scale, one IEEE float32 division, as kvq_write_cache
   a.k_inv = is_asym(cache->k_fmt) ? 1.0f : one / cache->k_scale;
   a.v_inv = is_asym(cache->v_fmt) ? 1.0f : one / cache->v_scale;
+  a.spin_limit = kDefaultSpinLimit;
+  a.withhold_cta = -1;
+  a.withhold_tile = -1;
+  if (g_wait_hook_armed.exchange(0) != 0) {
+    a.spin_limit = g_wait_hook_polls.load();
+    a.withhold_cta = g_wait_hook_cta.load();
+    a.withhold_tile = g_wait_hook_tile.load();
+  }
   cudaError_t e;
   const int kf = cache->k_fmt, vf = cache->v_fmt;
   if (is_asym(kf)) {
@@ -408,6 +426,15 @@ kvq_status kvq_calibrate_head_scales(const void* x, int64_t num_tokens, int32_t 
       launch_calibrate_heads(static_cast<const uint16_t*>(x), num_tokens, num_kv_heads, head_dim,
                              stride, qmax, scales_out, stream, sms);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_debug_arm_wait_timeout(int32_t polls, int32_t cta, int32_t tile) {
+  if (polls < 1 || cta < -1 || tile < -1) return KVQ_ERR_INVALID_ARGUMENT;
+  g_wait_hook_polls.store(polls);
+  g_wait_hook_cta.store(cta);
+  g_wait_hook_tile.store(tile);
+  g_wait_hook_armed.store(1);
+  return KVQ_OK;
 }
 
 kvq_status kvq_get_device_error(kvq_stream_t stream, uint32_t* bits) {

@@ -41,8 +41,8 @@
 
 namespace kvq {
 
-constexpr int kHeadsPerCta = 8;  // kv-heads (= consumer warps) per CTA
-constexpr int kSpinLimit = 1 << 26;  // polls of an mbarrier before giving up
+constexpr int kHeadsPerCta = kHeadsPerCtaHost;  // kv-heads (= consumer warps) per CTA
+constexpr int kSpinLimit = 1 << 22;  // default polls of an mbarrier before giving up
 
 template <int D_, int KF, int VF, bool KVARN>
 struct DecodeCfg {
@@ -85,12 +85,12 @@ struct DecodeCfg {
 // Shared memory of a CTA (bytes): the ring; per warp its query rows (G rows of
 // D bf16, filled ahead of each segment) and, with KVarN, a float row for the
 // query rotation; per stage a tile header and two mbarriers; a scratch area
-// with the producer's cursor; and 1 KB of alignment.
+// with the producer's cursor and the abort flag; and 1 KB of alignment.
 __host__ __device__ constexpr int q_rows_bytes(int g, int d) { return (g * d * 2 + 15) / 16 * 16; }
 template <class C>
 __host__ __device__ constexpr int decode_smem_bytes(int hpc, int g) {
   return C::STAGES * C::stage_bytes(hpc) + hpc * q_rows_bytes(g, C::D) + (C::KVARN_ ? hpc * C::D * 4 : 0) +
-         C::STAGES * 48 + 192 + 1024;
+         C::STAGES * 48 + 256 + 1024;
 }
 
 // Row of mma row r (0..15) of a tile: the QK row r holds token kRow[r].  With
@@ -245,10 +245,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for `parity` of an mbarrier, at most kSpinLimit polls; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int n = 0; n < kSpinLimit; ++n)
+// Wait for `parity` of an mbarrier, at most `limit` polls; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int limit) {
+  for (int n = 0; n < limit; ++n)
     if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// The same, giving up early once the CTA's abort flag (shared memory) is set;
+// the flag is read only after the first poll has failed.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, int limit,
+                                                   const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  for (int n = 1; n < limit; ++n) {
+    if ((n & 15) == 0 && *abort) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+  }
   return false;
 }
 // 4-D TMA tile load completing on mbarrier `bar`, with an L2 eviction policy
@@ -367,12 +378,6 @@ __device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
   uint16_t r;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
   return r;
-}
-__device__ __forceinline__ void bar_arrive(int id, int threads) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-__device__ __forceinline__ void bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -691,7 +696,13 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
   long long* scratch =
       reinterpret_cast<long long*>(smem + hdr_off + C::STAGES * (sizeof(TileHeader) + 16));
   // scratch: [0] T, [1] first sequence, [2] its first tile, [3] R1, [4..12) scan,
-  // [12..16) partial segments: (first tile, sequence << 32 | tiles) per end of the range
+  // [12..16) partial segments: (first tile, sequence << 32 | tiles) per end of the range,
+  // [16..21) producer cursor, [21] second page id, [22] abort flag (int),
+  // [23] withheld tile (int; test hook), [24] per end of the range: warps whose
+  // rows of the partial slot are stored (two ints)
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(scratch + 22);
+  int* const done_warps = reinterpret_cast<int*>(scratch + 24);
+  const int spin = a.spin_limit;
 
   // this warp's G query rows of sequence s -> shared memory (asynchronous)
   auto prefetch_q = [&](int s) {
@@ -794,6 +805,10 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
       mbar_init(empty_s + 8 * i, hpc);
     }
     for (int i = 12; i < 16; ++i) scratch[i] = -1;
+    *abort_flag = 0;
+    reinterpret_cast<int*>(scratch + 23)[0] =
+        (k == a.withhold_cta && hg == 0) ? a.withhold_tile : -1;
+    done_warps[0] = done_warps[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -866,7 +881,9 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     const int off = tok & bs_mask;
     const uint32_t sb = base_s + st * stage_bytes;
     const uint32_t bar = full_s + 8 * st;
-    if constexpr (split) {  // 8-token pages: the tile is two pages, each loaded as
+    // test hook: this tile's loads are never issued (its stage never fills)
+    if (u.i == reinterpret_cast<const int*>(scratch + 23)[0]) {
+    } else if constexpr (split) {  // 8-token pages: the tile is two pages, each loaded as
       // per-head 8-row boxes (rows 0-7, then 8-15 of the head's [16][row] box)
       // and [head][field][8] metadata boxes (the second meta_half bytes on)
       const bool two = second_half(u);
@@ -964,13 +981,26 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
   constexpr int E = 2 * C::DTILES;
   float Oa[E], Ob[E];
   int seg_t0 = 0;
-  bool healthy = true;
   bool first_seg = true;  // the range's first segment (slot 0 if partial; slot 1 otherwise)
 
+  // A wait that runs out (a tile that never lands, a warp that never arrives)
+  // raises KVQ_DEVERR_TIMEOUT and the abort flag: the producer issues nothing
+  // more, so every warp soon meets a wait that cannot complete, sees the flag
+  // there and leaves the loop; nothing is published, and the CTA returns once
+  // no copy it issued is in flight (below).
+  auto give_up = [&]() {
+    if (lane == 0) {
+      raise_error(16u);  // KVQ_DEVERR_TIMEOUT: the results of this launch are invalid
+      *abort_flag = 1;
+    }
+  };
   int st = 0;
   uint32_t phase = 0;
   for (int i = 0; i < n; ++i) {
-    if (!mbar_wait(full_s + 8 * st, phase)) healthy = false;
+    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(full_s + 8 * st, phase, spin, abort_flag))) {
+      give_up();
+      break;
+    }
     const TileHeader hd = hdr[st];
     const uint32_t sb = base_s + st * stage_bytes;
     const size_t out_row0 = static_cast<size_t>(hd.s) * a.num_q_heads + static_cast<size_t>(h) * G;
@@ -1136,8 +1166,12 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_s + 8 * st);
     if (threadIdx.x == 0 && cur->i < n) {  // refill this stage once every warp has read it
-      if (mbar_wait(empty_s + 8 * st, phase)) issue(st);
-      else raise_error(16u);  // KVQ_DEVERR_TIMEOUT
+      if (mbar_wait_or_abort(empty_s + 8 * st, phase, spin, abort_flag)) {
+        issue(st);
+      } else {
+        raise_error(16u);  // KVQ_DEVERR_TIMEOUT
+        *abort_flag = 1;
+      }
     }
     __syncwarp();
 
@@ -1217,7 +1251,6 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     if (!(hd.flags & 2)) continue;
 
     // ================= end of this CTA's segment of sequence hd.s =================
-    if (!healthy && lane == 0) raise_error(16u);  // KVQ_DEVERR_TIMEOUT (garbage results)
     float L0 = l0, L1 = l1, Z0 = z0, Z1 = z1;
 #pragma unroll
     for (int o = 4; o <= 16; o <<= 1) {
@@ -1263,18 +1296,22 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
       if (2 * c + 1 < G)
         *reinterpret_cast<float2*>(a.ws_ml + 2 * (slot + 2 * c + 1)) = make_float2(m1, L1);
     }
-    if (warp != pub) {
-      bar_arrive(1 + j, hpc * 32);  // hand the stores to the publishing warp; go on
-    } else {
-      bar_sync(1 + j, hpc * 32);
-      if (lane == 0) {
-        __threadfence();  // every warp's slot stores before the tag
+    // the last warp to store its rows publishes the slot: each warp counts
+    // itself in (the warp barrier orders its lanes' stores before lane 0's
+    // release), and the one that completes the count fences and stores the
+    // tag.  No warp waits for another, so a warp that gave up leaves the
+    // count short and the slot unpublished.
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(done_warps + j, 1) == hpc - 1) {
+        __threadfence();  // every warp's slot stores (seen through the count) before the tag
         st_relaxed_u64(a.tags + (static_cast<size_t>(k) * HG + hg) * 2 + j, a.epoch);
         scratch[12 + 2 * j] = hd.ps;
         scratch[13 + 2 * j] = (static_cast<long long>(hd.s) << 32) | hd.tiles;
       }
-      __syncwarp();
     }
+    __syncwarp();
   }
 
   // ---- merges.  A CTA with a partial segment checks the tags of the sequence's
@@ -1285,6 +1322,20 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
   // team's claim) into the slot of its first range, then the teams (by the team
   // merger that sees every team's tag and wins the sequence's claim).
   __syncthreads();
+  if (*abort_flag) {  // a wait gave up: publish and merge nothing; leave once the
+    // copies already issued have landed: each thread's query-row prefetch, and
+    // the bulk copies of the last STAGES tiles issued (the only ones that can
+    // still be in flight; a withheld tile was never issued)
+    cp_async_wait<0>();
+    if (threadIdx.x == 0) {
+      const int issued = cur->i;
+      for (int t = issued > C::STAGES ? issued - C::STAGES : 0; t < issued; ++t) {
+        if (t == reinterpret_cast<const int*>(scratch + 23)[0]) continue;
+        mbar_wait(full_s + 8 * (t % C::STAGES), (t / C::STAGES) & 1, spin);
+      }
+    }
+    return;
+  }
   const long long Tm = scratch[0];
   if (warp == pub) {
     __threadfence();

@@ -9,6 +9,8 @@ namespace kvq {
 
 // Most stream-K ranges (CTAs per head group) of one decode launch.
 constexpr int kMaxCtas = 65535;
+// Most kv-heads (consumer warps) per decode CTA.
+constexpr int kHeadsPerCtaHost = 8;
 
 struct WriteArgs {
   const uint16_t* key;    // bf16 bits
@@ -81,6 +83,13 @@ struct DecodeArgs {
   __half* v_meta_w;
   float k_inv;  // 1/k_scale (symmetric formats, per-tensor scales)
   float v_inv;
+  // Bounded pipeline waits: polls of an mbarrier before the CTA gives up (sets
+  // KVQ_DEVERR_TIMEOUT and returns).  Test hook: CTA (withhold_cta, head group
+  // 0) never issues the loads of its tile withhold_tile (-1: none), so that a
+  // wait runs out with nothing in flight.
+  int spin_limit;
+  int withhold_cta;
+  int withhold_tile;
 };
 
 cudaError_t launch_write(const WriteArgs& a, int head_dim, int kf, int vf, bool kvarn,

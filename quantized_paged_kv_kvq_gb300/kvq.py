@@ -66,6 +66,7 @@ SIGNATURES = {
     "kvq_hadamard": (_I32, [_P, _I32, _I64, _I32, _P, _I32, _P]),
     "kvq_calibrate_scale": (_I32, [_P, _I64, _F32, _P, _P]),
     "kvq_calibrate_head_scales": (_I32, [_P, _I64, _I32, _I32, _I64, _F32, _P, _P]),
+    "kvq_debug_arm_wait_timeout": (_I32, [_I32, _I32, _I32]),
     "kvq_get_device_error": (_I32, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "kvq_status_string": (ctypes.c_char_p, [_I32]),
     "kvq_version": (ctypes.c_char_p, []),
@@ -314,6 +315,14 @@ def kvq_calibrate_head_scales(x: torch.Tensor, qmax: float, out: torch.Tensor, s
                                        float(qmax), _ptr(out), _stream(stream))
     _check(st, "kvq_calibrate_head_scales")
     return out
+
+
+def kvq_debug_arm_wait_timeout(polls: int, cta: int, tile: int) -> None:
+    """Test hook: the next decode launch polls each pipeline wait at most `polls`
+    times, and CTA `cta` (first kv-head group) never loads its range's tile
+    `tile`, so that a wait runs out (KVQ_DEVERR_TIMEOUT); one launch only."""
+    _check(load_library().kvq_debug_arm_wait_timeout(polls, cta, tile),
+           "kvq_debug_arm_wait_timeout")
 
 
 def kvq_get_device_error(stream=None) -> int:

@@ -163,3 +163,11 @@ def test_hadamard_and_calibrate_validation(lib):
     assert lib.kvq_hadamard(None, 0, 0, 128, None, 0, None) == 0
     assert lib.kvq_calibrate_scale(FAKE, 10, 0.0, FAKE, None) == 1
     assert lib.kvq_calibrate_scale(FAKE, -1, 127.0, FAKE, None) == 1
+
+
+def test_wait_hook_validation(lib):
+    # only invalid settings here: a valid one would stay armed for the next launch
+    assert lib.kvq_debug_arm_wait_timeout(0, 0, 0) == 1
+    assert lib.kvq_debug_arm_wait_timeout(-5, 0, 0) == 1
+    assert lib.kvq_debug_arm_wait_timeout(100, -2, 0) == 1
+    assert lib.kvq_debug_arm_wait_timeout(100, 0, -3) == 1
