@@ -124,6 +124,57 @@ __device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
   return d;
 }
 
+// ---------------------------------------------------------------------------
+// Packed float32 pairs (sm_100 and later): one instruction computes two IEEE
+// float32 operations, each rounded to nearest exactly as the scalar operation
+// (no flush of subnormals), so they stand in for __fadd_rn / __fsub_rn /
+// __fmul_rn / __fmaf_rn pairwise without changing any result.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{ .reg .b64 pa, pb, pd; mov.b64 pa, {%2, %3}; mov.b64 pb, {%4, %5};"
+      " add.rn.f32x2 pd, pa, pb; mov.b64 {%0, %1}, pd; }"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{ .reg .b64 pa, pb, pd; mov.b64 pa, {%2, %3}; mov.b64 pb, {%4, %5};"
+      " sub.rn.f32x2 pd, pa, pb; mov.b64 {%0, %1}, pd; }"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{ .reg .b64 pa, pb, pd; mov.b64 pa, {%2, %3}; mov.b64 pb, {%4, %5};"
+      " mul.rn.f32x2 pd, pa, pb; mov.b64 {%0, %1}, pd; }"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// d = a * b + c, one rounding per lane
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{ .reg .b64 pa, pb, pc, pd; mov.b64 pa, {%2, %3}; mov.b64 pb, {%4, %5};"
+      " mov.b64 pc, {%6, %7}; fma.rn.f32x2 pd, pa, pb, pc; mov.b64 {%0, %1}, pd; }"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (c << 8) | (sat4(a) << 4) | sat4(b), sat4 = clamp to [0, 15]
+__device__ __forceinline__ uint32_t pack_sat_u4(int a, int b, uint32_t c) {
+  uint32_t d;
+  asm("cvt.pack.sat.u4.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// (c << 16) | (sat8(a) << 8) | sat8(b), sat8 = clamp to [0, 255]
+__device__ __forceinline__ uint32_t pack_sat_u8(int a, int b, uint32_t c) {
+  uint32_t d;
+  asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

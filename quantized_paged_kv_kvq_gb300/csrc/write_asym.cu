@@ -18,6 +18,9 @@ KVQ_ERROR_ACCESSOR(take_error_bits_write_asym)
 namespace {
 
 constexpr int kWriteWarps = 8;
+// Resident CTAs per SM each instance is compiled for (its register budget):
+// the KVarN rows need more registers.
+constexpr int ctas_per_sm(bool kvarn) { return kvarn ? 3 : 4; }
 
 // ---------------------------------------------------------------------------
 // Asymmetric formats (INT4 / UINT8 with a per-row scale and zero point), with
@@ -27,7 +30,10 @@ constexpr int kWriteWarps = 8;
 // stages and most of each reduction stay in registers.  The arithmetic is that
 // of the narrow row code (quantize_store, 8 elements per lane), in the same
 // order (fixed sum tree over groups of 8, butterfly stages h = 1, 2, ...,
-// D/2), so the codes are the same.
+// D/2), so the codes are the same.  Elementwise steps run on packed float32
+// pairs, and codes are packed by saturating conversions, which cuts the
+// instructions per element by about a third.  One warp per token; a pass
+// quantizes RPW consecutive rows of the token (its K heads, then its V heads).
 // ---------------------------------------------------------------------------
 template <int D>
 struct WideGeom {
@@ -62,18 +68,25 @@ __device__ __forceinline__ float tree_sum32(const float (&x)[32]) {
 
 // Butterfly stages h = 1 .. 16 in registers, then h = 32, 64 across the lanes
 // of the row (lane bit b set: other - v, else v + other; one fma with a +-1
-// factor is that same single rounding).
+// factor is that same single rounding).  Elements 2m and 2m+1 travel as a
+// packed pair, so every stage but h = 1 runs two butterflies per instruction.
 template <int D>
 __device__ __forceinline__ void fwht32(float (&v)[32], int sub) {
   constexpr int LPR = WideGeom<D>::LPR;
 #pragma unroll
-  for (int h = 1; h < 32; h <<= 1) {
+  for (int i = 0; i < 32; i += 2) {  // h = 1: inside a pair
+    const float x = v[i], y = v[i + 1];
+    v[i] = __fadd_rn(x, y);
+    v[i + 1] = __fsub_rn(x, y);
+  }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+  for (int h = 2; h < 32; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
       if ((i & h) == 0) {
-        const float x = v[i], y = v[i + h];
-        v[i] = __fadd_rn(x, y);
-        v[i + h] = __fsub_rn(x, y);
+        const float x0 = v[i], x1 = v[i + 1], y0 = v[i + h], y1 = v[i + h + 1];
+        add2(v[i], v[i + 1], x0, x1, y0, y1);
+        sub2(v[i + h], v[i + h + 1], x0, x1, y0, y1);
       }
     }
   }
@@ -81,20 +94,48 @@ __device__ __forceinline__ void fwht32(float (&v)[32], int sub) {
   for (int lo = 1; lo < LPR; lo <<= 1) {
     const float sgn = (sub & lo) ? -1.0f : 1.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float other = __shfl_xor_sync(0xffffffffu, v[i], lo);
-      v[i] = __fmaf_rn(sgn, v[i], other);
+    for (int i = 0; i < 32; i += 2) {
+      const float o0 = __shfl_xor_sync(0xffffffffu, v[i], lo);
+      const float o1 = __shfl_xor_sync(0xffffffffu, v[i + 1], lo);
+      fma2(v[i], v[i + 1], sgn, sgn, v[i], v[i + 1], o0, o1);
     }
   }
 }
 
+// Minimum and maximum of the 32 values (exact): four groups of 8 with
+// three-input operations, then the groups; short dependent chains, few live
+// values.
+__device__ __forceinline__ void minmax32(const float (&x)[32], float& mn, float& mx) {
+  float gmn[4], gmx[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const float* v = x + 8 * g;
+    gmn[g] = min3f(min3f(v[0], v[1], v[2]), min3f(v[3], v[4], v[5]), fminf(v[6], v[7]));
+    gmx[g] = max3f(max3f(v[0], v[1], v[2]), max3f(v[3], v[4], v[5]), fmaxf(v[6], v[7]));
+  }
+  mn = fminf(min3f(gmn[0], gmn[1], gmn[2]), gmn[3]);
+  mx = fmaxf(max3f(gmx[0], gmx[1], gmx[2]), gmx[3]);
+}
+
+// Shared-memory index (in pairs) of the rotation's diagonal pair m (elements
+// 2m, 2m+1) of a row of D: lane sub's pairs ml = 0..15 (m = 16 sub + ml) sit
+// at (ml / 2) * 2 LPR + 2 sub + ml % 2, so the 16-byte reads (two pairs) of
+// the row's LPR lanes fall on distinct banks.
+template <int D>
+__host__ __device__ constexpr int sign_pair_index(int m) {
+  constexpr int LPR = D / 32;
+  return (m % 16) / 2 * 2 * LPR + 2 * (m / 16) + m % 2;
+}
+
 // One row (token t, kv-head h) of an asymmetric format, 32 elements per lane.
+// sgn: the rotation's diagonal pairs (+-1.0f) in shared memory, offset to this
+// lane's first pair (sign_pair_index).
 template <int D, int F, bool KVARN>
 __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool active,
                                                   uint8_t* __restrict__ cache,
                                                   __half* __restrict__ meta, size_t row,
                                                   int64_t blk, int off, int h, int Hkv, int bs,
-                                                  uint32_t sign_bits, float cR) {
+                                                  const float2* sgn, float cR) {
   constexpr int LPR = WideGeom<D>::LPR;
   __half sig16 = __float2half_rn(1.0f);
   if constexpr (KVARN) {
@@ -102,30 +143,32 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
     const float mean = __fmul_rn(tree_sum32<D>(x), inv_d);
     float sq[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float dv = __fsub_rn(x[i], mean);
-      sq[i] = __fmul_rn(dv, dv);
+    for (int i = 0; i < 32; i += 2) {
+      float d0, d1;
+      sub2(d0, d1, x[i], x[i + 1], mean, mean);
+      mul2(sq[i], sq[i + 1], d0, d1, d0, d1);
     }
     const float var = __fmul_rn(tree_sum32<D>(sq), inv_d);
     sig16 = __float2half_rn(__fsqrt_rn(var));
     if (__half2float(sig16) == 0.0f) sig16 = __float2half_rn(1.0f);
     const float inv_sigma = __frcp_rn(__half2float(sig16));
+    // y = d . (x * (1/sigma)) = x * (d * (1/sigma)): a product by -1 is exact and
+    // rounding is symmetric in sign, so the two orders give the same bits
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float y = __fmul_rn(x[i], inv_sigma);
-      // d_i = -1: flip the sign bit (the exact negation, as one logic op)
-      x[i] = __uint_as_float(__float_as_uint(y) ^ ((sign_bits << (31 - i)) & 0x80000000u));
+    for (int i = 0; i < 32; i += 4) {
+      const float4 sp = *reinterpret_cast<const float4*>(sgn + (i / 4) * 2 * LPR);
+      float m0, m1, m2, m3;
+      mul2(m0, m1, sp.x, sp.y, inv_sigma, inv_sigma);
+      mul2(m2, m3, sp.z, sp.w, inv_sigma, inv_sigma);
+      mul2(x[i], x[i + 1], x[i], x[i + 1], m0, m1);
+      mul2(x[i + 2], x[i + 3], x[i + 2], x[i + 3], m2, m3);
     }
     fwht32<D>(x, sub);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], cR);
+    for (int i = 0; i < 32; i += 2) mul2(x[i], x[i + 1], x[i], x[i + 1], cR, cR);
   }
-  float mn = x[0], mx = x[0];
-#pragma unroll
-  for (int i = 1; i < 32; ++i) {
-    mn = fminf(mn, x[i]);
-    mx = fmaxf(mx, x[i]);
-  }
+  float mn, mx;
+  minmax32(x, mn, mx);
 #pragma unroll
   for (int o = LPR / 2; o >= 1; o >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
@@ -137,38 +180,49 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
   const __half z16 = __float2half_rn(mn);
   const float zf = __half2float(z16);
   const float inv_s = __frcp_rn(__half2float(s16));
-  // code = clamp(rne((x - z) * inv_s), 0, L): a saturating round-to-nearest-even
-  // conversion to u8 is rne then clamp to [0, 255]
-  uint32_t c[32];
+  // code = clamp(rne((x - z) * inv_s), 0, L): rne to int32, then the pack
+  // instruction's saturation to [0, L]; each word is packed as soon as its
+  // codes exist
+  auto code2 = [&](int i, int& c0, int& c1) {
+    float v0, v1;
+    sub2(v0, v1, x[i], x[i + 1], zf, zf);
+    mul2(v0, v1, v0, v1, inv_s, inv_s);
+    c0 = __float2int_rn(v0);
+    c1 = __float2int_rn(v1);
+  };
+  if constexpr (F == INT4A) {  // element 2i in the low nibble of byte i
+    uint32_t ww[4];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float v = __fmul_rn(__fsub_rn(x[i], zf), inv_s);
-    uint32_t q;
-    asm("cvt.rni.sat.u8.f32 %0, %1;" : "=r"(q) : "f"(v));
-    c[i] = L == 255 ? q : min(q, static_cast<uint32_t>(L));
-  }
-  if (active) {
-    if constexpr (F == INT4A) {
-      uint4 w;
-      uint32_t ww[4];
+    for (int k = 0; k < 4; ++k) {
+      int c0, c1;
+      code2(8 * k + 6, c0, c1);
+      uint32_t t = pack_sat_u4(c1, c0, 0u);
+      code2(8 * k + 4, c0, c1);
+      t = pack_sat_u4(c1, c0, t);
+      code2(8 * k + 2, c0, c1);
+      t = pack_sat_u4(c1, c0, t);
+      code2(8 * k, c0, c1);
+      ww[k] = pack_sat_u4(c1, c0, t);
+    }
+    if (active)
+      *reinterpret_cast<uint4*>(cache + row * (D / 2) + sub * 16) =
+          make_uint4(ww[0], ww[1], ww[2], ww[3]);
+  } else {  // element i in byte i
+    uint32_t ww[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t t = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t |= c[8 * k + i] << (4 * i);
-        ww[k] = t;
-      }
-      w.x = ww[0]; w.y = ww[1]; w.z = ww[2]; w.w = ww[3];
-      *reinterpret_cast<uint4*>(cache + row * (D / 2) + sub * 16) = w;
-    } else {
-      uint32_t ww[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        ww[k] = c[4 * k] | (c[4 * k + 1] << 8) | (c[4 * k + 2] << 16) | (c[4 * k + 3] << 24);
+    for (int k = 0; k < 8; ++k) {
+      int c0, c1, c2, c3;
+      code2(4 * k + 2, c2, c3);
+      code2(4 * k, c0, c1);
+      ww[k] = pack_sat_u8(c1, c0, pack_sat_u8(c3, c2, 0u));
+    }
+    if (active) {
       uint4* dst = reinterpret_cast<uint4*>(cache + row * D + sub * 32);
       dst[0] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
       dst[1] = make_uint4(ww[4], ww[5], ww[6], ww[7]);
     }
+  }
+  if (active) {
     if (sub == 0) {
       constexpr int NF = KVARN ? 3 : 2;
       __half* m = meta + ((static_cast<size_t>(blk) * Hkv + h) * NF) * bs + off;
@@ -179,11 +233,56 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
   }
 }
 
+// The rows r = p * RPW + (lane / LPR) of a token (its K heads, then its V
+// heads), held in x: quantized and stored.  reload(x) refills x with the
+// lane's input (a pass with both K and V rows quantizes x twice, and the
+// KVarN row code rotates x in place).
+template <int D, int KF, int VF, bool KVARN, class Reload>
+__device__ __forceinline__ void quantize_pass(float (&x)[32], const Reload& reload,
+                                              const WriteArgs& a, int r, int sub, size_t row0,
+                                              long long blk, int off, const float2* lane_sgn) {
+  const int Hkv = a.num_kv_heads;
+  const bool act = r < 2 * Hkv;
+  const bool is_v = r >= Hkv;
+  const int h = is_v ? r - Hkv : r;
+  if (__all_sync(0xffffffffu, !is_v || !act)) {
+    quantize_row_wide<D, KF, KVARN>(x, sub, act, a.k_cache, a.k_meta, row0 + h, blk, off, h, Hkv,
+                                    a.block_size, lane_sgn, a.cR);
+  } else if (__all_sync(0xffffffffu, is_v || !act)) {
+    quantize_row_wide<D, VF, KVARN>(x, sub, act, a.v_cache, a.v_meta, row0 + h, blk, off, h, Hkv,
+                                    a.block_size, lane_sgn, a.cR);
+  } else {  // a pass with K and V rows (fewer kv-heads than rows per pass)
+    quantize_row_wide<D, KF, KVARN>(x, sub, act && !is_v, a.k_cache, a.k_meta, row0 + h, blk, off,
+                                    h, Hkv, a.block_size, lane_sgn, a.cR);
+    if constexpr (KVARN) reload(x);  // the K rows were rotated in place
+    quantize_row_wide<D, VF, KVARN>(x, sub, act && is_v, a.v_cache, a.v_meta, row0 + h, blk, off,
+                                    h, Hkv, a.block_size, lane_sgn, a.cR);
+  }
+}
+
+// The rotation's diagonal as +-1.0f pairs in shared memory (sign_pair_index).
+template <int D, bool KVARN>
+__device__ __forceinline__ void fill_sign_pairs(float2* sgn, const int8_t* signs) {
+  if constexpr (KVARN) {
+    for (int m = threadIdx.x; m < D / 2; m += blockDim.x) {
+      float2 p = make_float2(1.0f, 1.0f);
+      if (signs != nullptr) {
+        p.x = signs[2 * m] < 0 ? -1.0f : 1.0f;
+        p.y = signs[2 * m + 1] < 0 ? -1.0f : 1.0f;
+      }
+      sgn[sign_pair_index<D>(m)] = p;
+    }
+    __syncthreads();
+  }
+}
+
+// One warp per token, loading each pass's rows straight from global memory.
 template <int D, int KF, int VF, bool KVARN>
-__global__ void __launch_bounds__(kWriteWarps * 32)
+__global__ void __launch_bounds__(kWriteWarps * 32, ctas_per_sm(KVARN))
     write_asym_kernel(WriteArgs a) {
-  constexpr int LPR = WideGeom<D>::LPR;
-  constexpr int RPW = WideGeom<D>::RPW;
+  constexpr int LPR = WideGeom<D>::LPR, RPW = WideGeom<D>::RPW;
+  __shared__ __align__(16) float2 sgn[KVARN ? D / 2 : 1];
+  fill_sign_pairs<D, KVARN>(sgn, a.signs);
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kWriteWarps + (threadIdx.x >> 5);
   if (t >= a.num_tokens) return;
@@ -197,66 +296,29 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
   const int off = static_cast<int>(slot & (a.block_size - 1));
   const int sub = lane % LPR, grp = lane / LPR;
   const int Hkv = a.num_kv_heads;
-
-  uint32_t sign_bits = 0;  // bit i: element sub*32 + i of the diagonal is -1
-  if constexpr (KVARN) {
-    if (a.signs != nullptr) {
-      const uint4* sp = reinterpret_cast<const uint4*>(a.signs + sub * 32);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint4 sv = sp[q];
-        const uint32_t w4[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int b = 0; b < 4; ++b)
-            sign_bits |= ((w4[k] >> (8 * b + 7)) & 1u) << (16 * q + 4 * k + b);
-      }
-    }
-  }
-
-  const uint16_t* krow = a.key + t * a.key_stride;
-  const uint16_t* vrow = a.value + t * a.value_stride;
+  const float2* lane_sgn = sgn + (KVARN ? sign_pair_index<D>(sub * 16) : 0);
   const size_t row0 = (static_cast<size_t>(blk) * a.block_size + off) * Hkv;
-  // rows of the token: K heads 0..Hkv-1, then V heads; RPW rows per pass
+  // this lane's 32 inputs of row r (K heads, then V heads) of the token
+  auto row_src = [&](int r) {
+    return (r < Hkv ? a.key + t * a.key_stride + static_cast<size_t>(r) * D
+                    : a.value + t * a.value_stride + static_cast<size_t>(r - Hkv) * D) + sub * 32;
+  };
   for (int r0 = 0; r0 < 2 * Hkv; r0 += RPW) {
     const int r = r0 + grp;
     const bool act = r < 2 * Hkv;
-    const bool is_v = r >= Hkv;
-    const int h = is_v ? r - Hkv : r;
-    uint4 raw[4];
-    const uint16_t* src = (is_v ? vrow : krow) + h * D + sub * 32;
+    const uint16_t* src = row_src(act ? r : 0);
+    auto load = [&](float (&y)[32]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) raw[q] = act ? ldg_stream16(src + 8 * q) : make_uint4(0, 0, 0, 0);
-    float x[32];
+      for (int q = 0; q < 4; ++q) {
+        float e[8];
+        unpack8(act ? ldg_stream16(src + 8 * q) : make_uint4(0, 0, 0, 0), e);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float e[8];
-      unpack8(raw[q], e);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[8 * q + i] = e[i];
-    }
-    if (__all_sync(0xffffffffu, !is_v || !act)) {
-      quantize_row_wide<D, KF, KVARN>(x, sub, act, a.k_cache, a.k_meta, row0 + h, blk, off, h,
-                                      Hkv, a.block_size, sign_bits, a.cR);
-    } else if (__all_sync(0xffffffffu, is_v || !act)) {
-      quantize_row_wide<D, VF, KVARN>(x, sub, act, a.v_cache, a.v_meta, row0 + h, blk, off, h,
-                                      Hkv, a.block_size, sign_bits, a.cR);
-    } else {  // a pass with K and V rows (fewer kv-heads than rows per pass)
-      quantize_row_wide<D, KF, KVARN>(x, sub, act && !is_v, a.k_cache, a.k_meta, row0 + h, blk,
-                                      off, h, Hkv, a.block_size, sign_bits, a.cR);
-      if constexpr (KVARN) {  // the K pass rotated x in place: the V rows start again
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float e[8];
-          unpack8(act ? ldg_stream16(src + 8 * q) : make_uint4(0, 0, 0, 0), e);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[8 * q + i] = e[i];
-        }
+        for (int i = 0; i < 8; ++i) y[8 * q + i] = e[i];
       }
-      quantize_row_wide<D, VF, KVARN>(x, sub, act && is_v, a.v_cache, a.v_meta, row0 + h, blk,
-                                      off, h, Hkv, a.block_size, sign_bits, a.cR);
-    }
+    };
+    float x[32];
+    load(x);
+    quantize_pass<D, KF, VF, KVARN>(x, load, a, r, sub, row0, blk, off, lane_sgn);
   }
 }
 
