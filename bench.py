@@ -728,6 +728,23 @@ def W_SEED(name):
     return W.SEEDS[name]
 
 
+def quantized_vs_bf16(per):
+    """Decode and write time of each 8-bit cache of the Llama-3-8B shape against
+    the unquantized 16-bit cache on the same shape and inputs (the comparison
+    the pages' FP8 / INT8 numbers are about), where both were measured."""
+    ref = per.get("llama8b_bf16")
+    if not ref:
+        return None
+    out = {"reference": "llama8b_bf16", "decode_us": ref["decode_us"],
+           "cache_write_us": ref["cache_write_us"]}
+    for name in ("llama8b_int8",):
+        if name in per:
+            out[name] = {"decode_us": per[name]["decode_us"],
+                         "decode_speedup": ref["decode_us"] / per[name]["decode_us"],
+                         "kv_bytes_ratio": per[name]["decode_bytes"] / ref["decode_bytes"]}
+    return out
+
+
 def run_kvq(args, rank: int, world: int, local_rank: int):
     import torch
     import torch.distributed as dist
@@ -822,6 +839,7 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
         "clocks": head["clocks"],
         "cpu_baseline": cpu,
         "workloads": {k: {kk: vv for kk, vv in v.items()} for k, v in per.items()},
+        "quantized_vs_bf16": quantized_vs_bf16(per),
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -59,6 +59,9 @@ typedef enum {
   KVQ_FMT_FP8_E5M2 = 3,   /* OCP E5M2 byte, one fp32 scale per tensor            */
   KVQ_FMT_INT4_ASYM = 4,  /* 4-bit code, fp16 scale + zero point per token-head  */
   KVQ_FMT_UINT8_ASYM = 5, /* 8-bit code, fp16 scale + zero point per token-head  */
+  KVQ_FMT_BF16 = 6,       /* the bf16 value itself, no scale (PR #4893 item 1's
+                             --kv-cache-dtype auto: the unquantized 16-bit cache);
+                             K and V both, no per-head scales, no rotation      */
 } kvq_format;
 
 /* KVarN pre-quantization (both tensors; asymmetric formats only): per
@@ -72,8 +75,9 @@ typedef enum {
  * Code arrays (passed separately to the calls):
  *   k_cache, v_cache: [num_blocks, block_size, num_kv_heads, row_bytes] bytes,
  *   row_bytes = head_dim for 8-bit formats, head_dim/2 for INT4 (element 2i
- *   in the low nibble of byte i, element 2i+1 in the high nibble); int8
- *   codes are two's complement.  16-byte aligned.
+ *   in the low nibble of byte i, element 2i+1 in the high nibble), 2*head_dim
+ *   for BF16 (little-endian bf16 values); int8 codes are two's complement.
+ *   16-byte aligned.
  * Metadata (asymmetric formats only, else NULL):
  *   k_meta, v_meta: fp16 [num_blocks, num_kv_heads, F, block_size] with
  *   F = 2 fields (scale, zero point) or 3 (scale, zero point, sigma) with
@@ -98,8 +102,8 @@ typedef struct {
   int32_t block_size;   /* tokens per block: 8, 16, 32, 64 or 128 */
   int32_t num_blocks;   /* >= 1 */
   uint32_t flags;       /* KVQ_FLAG_* */
-  float k_scale;        /* symmetric K formats: > 0 (1.0 = uncalibrated fp8) */
-  float v_scale;        /* symmetric V formats: > 0 */
+  float k_scale;        /* symmetric K formats: > 0 (1.0 = uncalibrated fp8); BF16: unused */
+  float v_scale;        /* symmetric V formats: > 0; BF16: unused */
   void* k_meta;
   void* v_meta;
   const int8_t* signs;
@@ -120,6 +124,7 @@ typedef struct {
  *   token; a slot past the cache sets KVQ_DEVERR_SLOT_RANGE and is skipped.
  *   Two tokens with the same slot: which one lands is unspecified.
  * Codes (fixed float32 arithmetic, IEEE round-to-nearest, no contraction):
+ *   BF16:  x itself (the input's 16 bits)
  *   INT8:  clamp(rint(x * inv), -128, 127), inv = 1.0f / scale
  *   FP8:   E4M3 / E5M2 of (x * inv), round to nearest even, saturating to
  *          the largest finite magnitude

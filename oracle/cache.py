@@ -37,6 +37,10 @@ def encode_rows(rows: np.ndarray, fmt: str, scale, kvarn: bool, signs):
     """Quantize rows [N, D] -> (codes [N, D'] uint8, meta [N, F] fp16 bits)."""
     rows = np.asarray(rows, np.float32)
     n = rows.shape[0]
+    if fmt == "bf16":  # the 16-bit cache stores the values themselves
+        if kvarn:
+            raise ValueError("the rotation is only defined with asymmetric formats")
+        return F.quant_bf16(rows), np.zeros((n, 0), np.uint16)
     if fmt in SYMMETRIC:
         if kvarn:
             raise ValueError("the rotation is only defined with asymmetric formats")
@@ -59,6 +63,8 @@ def encode_rows(rows: np.ndarray, fmt: str, scale, kvarn: bool, signs):
 def decode_rows(codes: np.ndarray, meta: np.ndarray, fmt: str, scale, kvarn: bool,
                 signs, head_dim: int) -> np.ndarray:
     """Dequantize stored rows back to float64 [N, D] (un-rotating for KVarN)."""
+    if fmt == "bf16":
+        return F.dequant_bf16(codes)
     if fmt in SYMMETRIC:
         return F.dequant_sym(codes, fmt, scale)
     c = F.unpack_int4(codes) if fmt == "int4_asym" else np.asarray(codes, np.uint8)

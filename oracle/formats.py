@@ -250,6 +250,28 @@ def dequant_asym(codes_unpacked, s, z) -> np.ndarray:
     return c * np.asarray(s, np.float64)[..., None] + np.asarray(z, np.float64)[..., None]
 
 
+# ---------------------------------------------------------------------------
+# The unquantized 16-bit cache (PR #4893 item 1: --kv-cache-dtype auto keeps
+# the model's 16-bit KV; here bfloat16, the write path's input type)
+# ---------------------------------------------------------------------------
+def quant_bf16(x) -> np.ndarray:
+    """Stored bytes of bf16-valued float32 inputs: the value's own 16 bits,
+    little-endian, two bytes per element (no scale, no rounding: the inputs
+    are bf16 already)."""
+    x = np.ascontiguousarray(x, np.float32)
+    bits = (x.view(np.uint32) >> 16).astype("<u2")
+    if np.any((x.view(np.uint32) & 0xFFFF) != 0):
+        raise ValueError("bf16 cache input must be bf16 values")
+    return bits.view(np.uint8).reshape(x.shape[:-1] + (2 * x.shape[-1],))
+
+
+def dequant_bf16(codes) -> np.ndarray:
+    """Values of stored bf16 rows (bytes [..., 2D]) as float64 [..., D]."""
+    c = np.ascontiguousarray(codes, np.uint8)
+    bits = c.view("<u2").astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
+
+
 def bytes_per_row(fmt: str, head_dim: int) -> int:
     """Stored code bytes per (token, kv-head)."""
     return head_dim // 2 if fmt == "int4_asym" else head_dim * (2 if fmt == "bf16" else 1)

@@ -19,13 +19,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool valid_fmt(int f) { return f >= KVQ_FMT_INT8 && f <= KVQ_FMT_UINT8_ASYM; }
+bool valid_fmt(int f) { return f >= KVQ_FMT_INT8 && f <= KVQ_FMT_BF16; }
 
+// Families that share a kernel: per-tensor-scaled 8-bit codes, per-row
+// asymmetric codes (optionally KVarN), and the 16-bit cache (K and V both).
 bool pairing_ok(int kf, int vf, bool kvarn) {
+  if ((kf == KVQ_FMT_BF16) != (vf == KVQ_FMT_BF16)) return false;
   const bool ak = is_asym(kf), av = is_asym(vf);
   if (kvarn) return ak && av;
   return ak == av;
 }
+bool scaled(int f) { return !is_asym(f) && f != KVQ_FMT_BF16; }
 
 // Checks shared by write and decode on the cache description.
 kvq_status check_cache(const kvq_cache_desc* c) {
@@ -42,19 +46,19 @@ kvq_status check_cache(const kvq_cache_desc* c) {
     return KVQ_ERR_UNSUPPORTED;
   const bool kvarn = (c->flags & KVQ_FLAG_VARNORM_ROTATE) != 0;
   if (!pairing_ok(c->k_fmt, c->v_fmt, kvarn)) return KVQ_ERR_UNSUPPORTED;
-  if (!is_asym(c->k_fmt) && !(c->k_scale > 0.0f && isfinite(c->k_scale)))
+  if (scaled(c->k_fmt) && !(c->k_scale > 0.0f && isfinite(c->k_scale)))
     return KVQ_ERR_INVALID_ARGUMENT;
-  if (!is_asym(c->v_fmt) && !(c->v_scale > 0.0f && isfinite(c->v_scale)))
+  if (scaled(c->v_fmt) && !(c->v_scale > 0.0f && isfinite(c->v_scale)))
     return KVQ_ERR_INVALID_ARGUMENT;
   if (is_asym(c->k_fmt) && (c->k_meta == nullptr || !aligned(c->k_meta, 16)))
     return KVQ_ERR_INVALID_ARGUMENT;
   if (is_asym(c->v_fmt) && (c->v_meta == nullptr || !aligned(c->v_meta, 16)))
     return KVQ_ERR_INVALID_ARGUMENT;
   if (kvarn && c->signs != nullptr && !aligned(c->signs, 16)) return KVQ_ERR_INVALID_ARGUMENT;
-  // per-kv-head scales: symmetric formats only
-  if (c->k_head_scales != nullptr && (is_asym(c->k_fmt) || !aligned(c->k_head_scales, 4)))
+  // per-kv-head scales: scaled symmetric formats only
+  if (c->k_head_scales != nullptr && (!scaled(c->k_fmt) || !aligned(c->k_head_scales, 4)))
     return KVQ_ERR_INVALID_ARGUMENT;
-  if (c->v_head_scales != nullptr && (is_asym(c->v_fmt) || !aligned(c->v_head_scales, 4)))
+  if (c->v_head_scales != nullptr && (!scaled(c->v_fmt) || !aligned(c->v_head_scales, 4)))
     return KVQ_ERR_INVALID_ARGUMENT;
   return KVQ_OK;
 }
@@ -77,11 +81,13 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 
 int heads_per_cta(int hkv) { return hkv < 8 ? hkv : 8; }
 
-// Stream-K ranges per head group: two resident CTAs per SM (the decode
-// kernel's shared-memory and register budget), at most one per possible tile.
-int auto_ctas(int num_seqs, int max_ctx, int head_groups, int sms) {
+// Stream-K ranges per head group: as many as the decode kernel has resident
+// CTAs (two per SM; one for the 16-bit cache, whose 64 KB stages fill an
+// SM's shared memory), at most one per possible tile.
+int auto_ctas(int num_seqs, int max_ctx, int head_groups, int sms, int per_sm) {
   const long long tiles_max = static_cast<long long>(num_seqs) * ((max_ctx + 15) / 16);
-  long long nc = (static_cast<long long>(sms > 0 ? sms : 152) * 2 + head_groups - 1) / head_groups;
+  long long nc =
+      (static_cast<long long>(sms > 0 ? sms : 152) * per_sm + head_groups - 1) / head_groups;
   if (nc > tiles_max) nc = tiles_max;
   if (nc > kMaxCtas) nc = kMaxCtas;
   return static_cast<int>(nc < 1 ? 1 : nc);
@@ -138,7 +144,7 @@ kvq_status decode_shape(const kvq_cache_desc* c, int32_t num_seqs, int32_t num_q
     const int sms = sm_count();
     if (sms <= 0) return KVQ_ERR_CUDA;
     nc = auto_ctas(num_seqs, max_context_len, c->num_kv_heads / heads_per_cta(c->num_kv_heads),
-                   sms);
+                   sms, c->k_fmt == KVQ_FMT_BF16 ? 1 : 2);
   }
   *NC = nc;
   return KVQ_OK;
@@ -195,8 +201,8 @@ kvq_status kvq_write_cache(const kvq_cache_desc* cache, void* k_cache, void* v_c
   a.num_blocks = cache->num_blocks;
   // inv = 1/scale, one IEEE float32 division on the host
   volatile float one = 1.0f;
-  a.k_inv = is_asym(cache->k_fmt) ? 1.0f : one / cache->k_scale;
-  a.v_inv = is_asym(cache->v_fmt) ? 1.0f : one / cache->v_scale;
+  a.k_inv = scaled(cache->k_fmt) ? one / cache->k_scale : 1.0f;
+  a.v_inv = scaled(cache->v_fmt) ? one / cache->v_scale : 1.0f;
   a.k_head_scale = cache->k_head_scales;
   a.v_head_scale = cache->v_head_scales;
   a.signs = cache->signs;
@@ -291,8 +297,8 @@ kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const v
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.max_context_len = max_context_len;
   a.num_ctas = NC;
-  a.qk_scale = sm_scale * kLog2e * (is_asym(cache->k_fmt) ? 1.0f : cache->k_scale);
-  a.v_scale = is_asym(cache->v_fmt) ? 1.0f : cache->v_scale;
+  a.qk_scale = sm_scale * kLog2e * (scaled(cache->k_fmt) ? cache->k_scale : 1.0f);
+  a.v_scale = scaled(cache->v_fmt) ? cache->v_scale : 1.0f;
   a.qk_base = sm_scale * kLog2e;
   a.k_head_scale = cache->k_head_scales;
   a.v_head_scale = cache->v_head_scales;
@@ -307,8 +313,8 @@ kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const v
   a.k_meta_w = append ? static_cast<__half*>(cache->k_meta) : nullptr;
   a.v_meta_w = append ? static_cast<__half*>(cache->v_meta) : nullptr;
   volatile float one = 1.0f;  // 1/scale, one IEEE float32 division, as kvq_write_cache
-  a.k_inv = is_asym(cache->k_fmt) ? 1.0f : one / cache->k_scale;
-  a.v_inv = is_asym(cache->v_fmt) ? 1.0f : one / cache->v_scale;
+  a.k_inv = scaled(cache->k_fmt) ? one / cache->k_scale : 1.0f;
+  a.v_inv = scaled(cache->v_fmt) ? one / cache->v_scale : 1.0f;
   a.spin_limit = kDefaultSpinLimit;
   a.withhold_cta = -1;
   a.withhold_tile = -1;
@@ -319,7 +325,9 @@ kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const v
   }
   cudaError_t e;
   const int kf = cache->k_fmt, vf = cache->v_fmt;
-  if (is_asym(kf)) {
+  if (kf == KVQ_FMT_BF16) {
+    e = launch_decode_bf16(a, cache->head_dim, stream);
+  } else if (is_asym(kf)) {
     e = cache->head_dim == 64 ? launch_decode_d64_asym(a, kf, vf, kvarn, stream)
                               : launch_decode_d128_asym(a, kf, vf, kvarn, stream);
   } else {
@@ -445,7 +453,8 @@ kvq_status kvq_get_device_error(kvq_stream_t stream, uint32_t* bits) {
                                       take_error_bits_decode_d64_sym,
                                       take_error_bits_decode_d128_sym,
                                       take_error_bits_decode_d64_asym,
-                                      take_error_bits_decode_d128_asym};
+                                      take_error_bits_decode_d128_asym,
+                                      take_error_bits_decode_bf16};
   for (auto f : take)
     if (f(&v) != cudaSuccess) return KVQ_ERR_CUDA;
   *bits = v;

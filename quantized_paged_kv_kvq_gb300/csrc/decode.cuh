@@ -63,7 +63,9 @@ struct DecodeCfg {
   static constexpr int K_HEAD = 16 * KB;  // bytes of one head's 16-token box
   static constexpr int V_HEAD = 16 * VB;
   // swizzle of the TMA boxes: 16-byte chunk index ^= address bits [7, 7+n)
-  static constexpr int swz_bits(int rb) { return rb == 128 ? 3 : rb == 64 ? 2 : 0; }
+  // (a 256-byte row of 16-bit values is loaded as two 128-byte halves, each a
+  // swizzle row, so it takes the 128-byte swizzle too)
+  static constexpr int swz_bits(int rb) { return rb >= 128 ? 3 : rb == 64 ? 2 : 0; }
   static constexpr int K_SWZ = swz_bits(KB);
   static constexpr int V_SWZ = swz_bits(VB);
   static constexpr int align(int x) { return (x + 1023) / 1024 * 1024; }
@@ -77,6 +79,7 @@ struct DecodeCfg {
   }
   static constexpr int STAGE_MAX = stage_bytes(kHeadsPerCta);
   static constexpr int STAGES = STAGE_MAX >= 24576 ? 3 : STAGE_MAX >= 16384 ? 5 : 6;
+  static constexpr int EB = KF == BF16 ? 2 : 1;  // K element bytes (INT4: see kslot_d)
   static constexpr bool KVARN_ = KVARN;
   static_assert(KW * 4 == K_LANE && VW * 4 == VPS, "layout");
   static_assert(KMF == VMF || KMF == 0 || VMF == 0, "one metadata row layout for K and V");
@@ -110,10 +113,11 @@ __device__ __forceinline__ int v_token(int c, int u) { return tile_row(c + 8 * (
 template <int D, int KF>
 __device__ __forceinline__ int kslot_d(int c, int j, int e) {
   using C = DecodeCfg<D, KF, INT8, false>;
-  if constexpr (KF != INT4A) {
-    constexpr int WPP = C::KPS / 4;
+  if constexpr (KF != INT4A) {  // 4 consecutive elements per k-step and lane
+    constexpr int EB = C::EB;
+    constexpr int WPP = C::KPS / (4 * EB);  // k-steps per load piece
     const int piece = j / WPP, within = j % WPP;
-    return piece * C::KSTRIDE_P + c * C::KPS + 4 * within + e;
+    return (piece * C::KSTRIDE_P + c * C::KPS + 4 * EB * within) / EB + e;
   } else {
     const int eb = 2 * (c * C::KPS + 4 * (j >> 1));
     const int ev = (e == 0) ? 0 : (e == 1) ? 4 : (e == 2) ? 1 : 5;
@@ -142,6 +146,11 @@ __device__ __forceinline__ void k_frag(const uint32_t (&kw)[2][KW], int j, uint3
     a2 = e4m3x2_to_f16x2(kw[0][j] >> 16);
     a1 = e4m3x2_to_f16x2(kw[1][j] & 0xFFFFu);
     a3 = e4m3x2_to_f16x2(kw[1][j] >> 16);
+  } else if constexpr (KF == BF16) {  // the values themselves, two per word
+    a0 = kw[0][2 * j];
+    a2 = kw[0][2 * j + 1];
+    a1 = kw[1][2 * j];
+    a3 = kw[1][2 * j + 1];
   } else if constexpr (KF == E5M2) {
     a0 = prmt(kw[0][j], 0u, 0x1404);
     a2 = prmt(kw[0][j], 0u, 0x3424);
@@ -165,6 +174,9 @@ __device__ __forceinline__ void v_pair(uint32_t wa, uint32_t wb, int i, uint32_t
     const uint32_t w = (i & 1) ? (pr >> 8) : pr;
     rg = hsub2_u32(and_or(w, 0x000F000Fu, 0x64006400u), 0x64006400u);
     rg8 = hsub2_u32(and_or(w, 0x00F000F0u, 0x54005400u), 0x54005400u);
+  } else if constexpr (VF == BF16) {  // word i holds dims 2i, 2i+1 of the token
+    rg = prmt(wa, wb, 0x5410);
+    rg8 = prmt(wa, wb, 0x7632);
   } else {
     const uint32_t il = (i & 1) ? prmt(wa, wb, 0x7362) : prmt(wa, wb, 0x5140);
     if constexpr (VF == E4M3) {
@@ -185,7 +197,7 @@ __device__ __forceinline__ void v_pair(uint32_t wa, uint32_t wb, int i, uint32_t
 template <int VF, int VW>
 __device__ __forceinline__ void v_frag(const uint32_t (&vw)[4][VW], int i, uint32_t& a0,
                                        uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-  const int m = (VF == INT4A) ? (i >> 2) : (i >> 1);
+  const int m = (VF == INT4A) ? (i >> 2) : (VF == BF16) ? i : (i >> 1);
   v_pair<VF>(vw[0][m], vw[1][m], i, a0, a1);
   v_pair<VF>(vw[2][m], vw[3][m], i, a2, a3);
 }
@@ -273,6 +285,31 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
       : "memory");
 }
+// The same for a 5-D tensor map (rows of 16-bit values seen as two 128-byte halves).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, int v, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar),
+      "l"(policy)
+      : "memory");
+}
+// Codes of one tile: the row-major maps are 4-D (row, head, token, block) per
+// head or (row, token, head, block) head-major; rows over 128 bytes add a
+// leading half-row dimension (two 128-byte halves, each a swizzle row).
+template <int RB>
+__device__ __forceinline__ void tma_codes_head(uint32_t dst, const CUtensorMap* map, int head,
+                                               int tok, int blk, uint32_t bar, uint64_t pol) {
+  if constexpr (RB > 128) tma_load_5d(dst, map, 0, 0, head, tok, blk, bar, pol);
+  else tma_load_4d(dst, map, 0, head, tok, blk, bar, pol);
+}
+template <int RB>
+__device__ __forceinline__ void tma_codes_heads(uint32_t dst, const CUtensorMap* map, int tok,
+                                                int head0, int blk, uint32_t bar, uint64_t pol) {
+  if constexpr (RB > 128) tma_load_5d(dst, map, 0, 0, tok, head0, blk, bar, pol);
+  else tma_load_4d(dst, map, 0, tok, head0, blk, bar, pol);
+}
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -335,15 +372,35 @@ __device__ __forceinline__ void fwht_accum_rows(float (&v)[E], int g) {
   }
 }
 
-// mma16816 with the accumulator given as four separate floats
+// mma16816 with the accumulator given as four separate floats; BF: both
+// operands bf16 (the 16-bit cache), else both fp16
+template <bool BF = false>
 __device__ __forceinline__ void mma16816(float& c0, float& c1, float& c2, float& c3, uint32_t a0,
                                          uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (BF) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c0), "+f"(c1), "+f"(c2), "+f"(c3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// two operands of an mma in the cache's 16-bit type (bf16 for the 16-bit
+// cache, else fp16), rounded to nearest
+template <bool BF>
+__device__ __forceinline__ uint32_t pack_op2(float lo, float hi) {
+  return BF ? pack_bf162(lo, hi) : pack_half2(lo, hi);
 }
 
 // The producer's position in the range.
@@ -664,7 +721,7 @@ __device__ __forceinline__ void append_new_tokens(const DecodeArgs& a, long long
 // SPLIT: pages of 8 tokens (a tile is two pages); a separate instance, so that
 // the other page sizes keep the one-box path's registers.
 template <int D, int KF, int VF, bool KVARN, bool SPLIT>
-__global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
+__global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
     decode_partition_kernel(const DecodeArgs a, const __grid_constant__ DecodeMaps maps) {
   using C = DecodeCfg<D, KF, VF, KVARN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -896,10 +953,10 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
       for (int hf = 0; hf < (two ? 2 : 1); ++hf) {
         const int b = hf ? blk2 : blk;
         for (int hh = 0; hh < hpc; ++hh) {
-          tma_load_4d(sb + hh * C::K_HEAD + hf * 8 * C::KB, &maps.k, 0, hg * hpc + hh, 0, b, bar,
-                      pol);
-          tma_load_4d(sb + v_off + hh * C::V_HEAD + hf * 8 * C::VB, &maps.v, 0, hg * hpc + hh, 0, b,
-                      bar, pol);
+          tma_codes_head<C::KB>(sb + hh * C::K_HEAD + hf * 8 * C::KB, &maps.k, hg * hpc + hh, 0, b,
+                                bar, pol);
+          tma_codes_head<C::VB>(sb + v_off + hh * C::V_HEAD + hf * 8 * C::VB, &maps.v,
+                                hg * hpc + hh, 0, b, bar, pol);
         }
         if constexpr (C::KMF > 0)
           tma_load_4d(sb + m_off + hf * C::meta_half(hpc, C::KMF), &maps.km, 0, 0, hg * hpc, b, bar,
@@ -911,12 +968,13 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     } else {  // one box per tile (pages of 16 or more tokens)
       mbar_arrive_expect(bar, tile_bytes);
       if (a.one_box) {
-        tma_load_4d(sb, &maps.k, 0, off, hg * hpc, blk, bar, pol);
-        tma_load_4d(sb + v_off, &maps.v, 0, off, hg * hpc, blk, bar, pol);
+        tma_codes_heads<C::KB>(sb, &maps.k, off, hg * hpc, blk, bar, pol);
+        tma_codes_heads<C::VB>(sb + v_off, &maps.v, off, hg * hpc, blk, bar, pol);
       } else {
         for (int hh = 0; hh < hpc; ++hh) {
-          tma_load_4d(sb + hh * C::K_HEAD, &maps.k, 0, hg * hpc + hh, off, blk, bar, pol);
-          tma_load_4d(sb + v_off + hh * C::V_HEAD, &maps.v, 0, hg * hpc + hh, off, blk, bar, pol);
+          tma_codes_head<C::KB>(sb + hh * C::K_HEAD, &maps.k, hg * hpc + hh, off, blk, bar, pol);
+          tma_codes_head<C::VB>(sb + v_off + hh * C::V_HEAD, &maps.v, hg * hpc + hh, off, blk, bar,
+                                pol);
         }
       }
       if constexpr (C::KMF > 0) tma_load_4d(sb + m_off, &maps.km, off, 0, hg * hpc, blk, bar, pol);
@@ -1044,14 +1102,16 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             v[e] = 0.0f;
-            if (g < G)
-              v[e] = __half2float(__float2half_rn(__uint_as_float(
-                  static_cast<uint32_t>(lds_u16(qbuf_s + 2 * (g * D + kslot_d<D, KF>(c, j, e)))) << 16)));
+            if (g < G) {
+              v[e] = __uint_as_float(
+                  static_cast<uint32_t>(lds_u16(qbuf_s + 2 * (g * D + kslot_d<D, KF>(c, j, e)))) << 16);
+              if constexpr (KF != BF16) v[e] = __half2float(__float2half_rn(v[e]));
+            }
             qs += v[e];
             if (e >= 2) qh += v[e];
           }
-          qf[j][0] = pack_half2(v[0], v[1]);
-          qf[j][1] = pack_half2(v[2], v[3]);
+          qf[j][0] = pack_op2<KF == BF16>(v[0], v[1]);  // exact (bf16 or its fp16 rounding)
+          qf[j][1] = pack_op2<KF == BF16>(v[2], v[3]);
         }
       }
       __syncwarp();  // every lane has read the rows: fetch the next segment's
@@ -1115,8 +1175,8 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     for (int j = 0; j < C::KSTEPS; ++j) {
       uint32_t a0, a1, a2, a3;
       k_frag<KF, C::KW>(kw, j, a0, a1, a2, a3);
-      if (j & 1) mma16816(sbb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
-      else mma16816(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+      if (j & 1) mma16816<KF == BF16>(sbb[0], sbb[1], sbb[2], sbb[3], a0, a1, a2, a3, qf[j][0], qf[j][1]);
+      else mma16816<KF == BF16>(sa[0], sa[1], sa[2], sa[3], a0, a1, a2, a3, qf[j][0], qf[j][1]);
     }
     float sl[4];
     {
@@ -1147,6 +1207,12 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
       if constexpr (C::VPS == 16) {
         const uint4 w = lds128(sb + v_addr[u]);
         vw[u][0] = w.x; vw[u][1] = w.y; vw[u][2] = w.z; vw[u][3] = w.w;
+      } else if constexpr (C::VPS == 32) {  // 16-bit values: chunks 2g and 2g+1, whose
+        // swizzled addresses differ in bit 4 only (same 128-byte row)
+        const uint4 w0 = lds128(sb + v_addr[u]);
+        const uint4 w1 = lds128(sb + (v_addr[u] ^ 16u));
+        vw[u][0] = w0.x; vw[u][1] = w0.y; vw[u][2] = w0.z; vw[u][3] = w0.w;
+        vw[u][4] = w1.x; vw[u][5] = w1.y; vw[u][6] = w1.z; vw[u][7] = w1.w;
       } else if constexpr (C::VPS == 8) {
         const uint2 w = lds64(sb + v_addr[u]);
         vw[u][0] = w.x; vw[u][1] = w.y;
@@ -1228,8 +1294,8 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
       pr[2] *= vs1; pr[3] *= vs1;
     }
     // ---- P^T operand: lane (g, c) needs head g at its 4 V tokens
-    const uint32_t x0 = pack_half2(pr[0], pr[2]);  // head 2c, rows (g, g+8)
-    const uint32_t x1 = pack_half2(pr[1], pr[3]);  // head 2c+1
+    const uint32_t x0 = pack_op2<VF == BF16>(pr[0], pr[2]);  // head 2c, rows (g, g+8)
+    const uint32_t x1 = pack_op2<VF == BF16>(pr[1], pr[3]);  // head 2c+1
     const int src0 = c * 4 + (g >> 1), src1 = (c + 4) * 4 + (g >> 1);
     const uint32_t u0 = __shfl_sync(0xffffffffu, x0, src0);
     const uint32_t u1 = __shfl_sync(0xffffffffu, x1, src0);
@@ -1242,7 +1308,8 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, 2)
     for (int d = 0; d < C::DTILES; ++d) {
       uint32_t a0, a1, a2, a3;
       v_frag<VF, C::VW>(vw, d, a0, a1, a2, a3);
-      mma16816(Oa[2 * d], Ob[2 * d], Oa[2 * d + 1], Ob[2 * d + 1], a0, a1, a2, a3, b0, b1);
+      mma16816<VF == BF16>(Oa[2 * d], Ob[2 * d], Oa[2 * d + 1], Ob[2 * d + 1], a0, a1, a2, a3, b0,
+                           b1);
     }
     if (++st == C::STAGES) {
       st = 0;

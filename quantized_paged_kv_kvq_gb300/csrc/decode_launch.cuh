@@ -31,9 +31,22 @@ inline CUtensorMapSwizzle swizzle_mode(int bits) {
 }
 
 // Codes [NB, bs, Hkv, row] bytes: dims (row, Hkv, bs, NB), box = one head's
-// 16 tokens (8 with 8-token pages: one page).
+// 16 tokens (8 with 8-token pages: one page).  A row over 128 bytes (16-bit
+// values) is two 128-byte halves: dims (128, 2, Hkv, bs, NB).
 inline bool encode_codes_map(CUtensorMap* m, const void* base, int row, int hkv, int bs, int nb,
                              int swz_bits) {
+  if (row > 128) {
+    const cuuint64_t dims[5] = {128, cuuint64_t(row / 128), cuuint64_t(hkv), cuuint64_t(bs),
+                                cuuint64_t(nb)};
+    const cuuint64_t strides[4] = {128, cuuint64_t(row), cuuint64_t(row) * hkv,
+                                   cuuint64_t(row) * hkv * bs};
+    const cuuint32_t box[5] = {128, cuuint32_t(row / 128), 1, cuuint32_t(bs < 16 ? bs : 16), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swizzle_mode(swz_bits), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const cuuint64_t dims[4] = {cuuint64_t(row), cuuint64_t(hkv), cuuint64_t(bs), cuuint64_t(nb)};
   const cuuint64_t strides[3] = {cuuint64_t(row), cuuint64_t(row) * hkv,
                                  cuuint64_t(row) * hkv * bs};
@@ -51,6 +64,18 @@ inline bool encode_codes_map(CUtensorMap* m, const void* base, int row, int hkv,
 // inside the cache; if the encoder rejects the ordering, per-head boxes are used.
 inline bool encode_codes_map_headmajor(CUtensorMap* m, const void* base, int row, int hkv, int bs,
                                        int nb, int hpc, int swz_bits) {
+  if (row > 128) {  // two 128-byte halves per row: dims (128, 2, bs, Hkv, NB)
+    const cuuint64_t dims[5] = {128, cuuint64_t(row / 128), cuuint64_t(bs), cuuint64_t(hkv),
+                                cuuint64_t(nb)};
+    const cuuint64_t strides[4] = {128, cuuint64_t(row) * hkv, cuuint64_t(row),
+                                   cuuint64_t(row) * hkv * bs};
+    const cuuint32_t box[5] = {128, cuuint32_t(row / 128), 16, cuuint32_t(hpc), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                swizzle_mode(swz_bits), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const cuuint64_t dims[4] = {cuuint64_t(row), cuuint64_t(bs), cuuint64_t(hkv), cuuint64_t(nb)};
   const cuuint64_t strides[3] = {cuuint64_t(row) * hkv, cuuint64_t(row),
                                  cuuint64_t(row) * hkv * bs};

@@ -12,10 +12,12 @@
 
 namespace kvq {
 
-enum Fmt : int { INT8 = 1, E4M3 = 2, E5M2 = 3, INT4A = 4, UINT8A = 5 };
+enum Fmt : int { INT8 = 1, E4M3 = 2, E5M2 = 3, INT4A = 4, UINT8A = 5, BF16 = 6 };
 
 __host__ __device__ constexpr bool is_asym(int f) { return f == INT4A || f == UINT8A; }
-__host__ __device__ constexpr int row_bytes(int f, int d) { return f == INT4A ? d / 2 : d; }
+__host__ __device__ constexpr int row_bytes(int f, int d) {
+  return f == INT4A ? d / 2 : f == BF16 ? 2 * d : d;
+}
 __host__ __device__ constexpr int asym_levels(int f) { return f == INT4A ? 15 : 255; }
 
 // Per-device error word (bits KVQ_DEVERR_*), one per translation unit (no

@@ -104,6 +104,7 @@ cudaError_t launch_decode_d64_asym(const DecodeArgs& a, int kf, int vf, bool kva
                                    cudaStream_t st);
 cudaError_t launch_decode_d128_asym(const DecodeArgs& a, int kf, int vf, bool kvarn,
                                     cudaStream_t st);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st);
 
 // read-and-clear of each translation unit's device error word
 cudaError_t take_error_bits_write(unsigned* bits);
@@ -112,6 +113,7 @@ cudaError_t take_error_bits_decode_d64_sym(unsigned* bits);
 cudaError_t take_error_bits_decode_d128_sym(unsigned* bits);
 cudaError_t take_error_bits_decode_d64_asym(unsigned* bits);
 cudaError_t take_error_bits_decode_d128_asym(unsigned* bits);
+cudaError_t take_error_bits_decode_bf16(unsigned* bits);
 
 cudaError_t launch_hadamard(void* x, int dtype, int64_t rows, int head_dim, const int8_t* signs,
                             int inverse, float cR, cudaStream_t st);

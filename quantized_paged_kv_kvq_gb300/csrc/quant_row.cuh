@@ -77,7 +77,14 @@ __device__ __forceinline__ void quantize_store(float (&x)[8], bool active, int h
                                                int off, int Hkv, int bs, uint32_t sign_bits,
                                                float cR) {
   constexpr int LPR = RowGeom<D>::LPR;
-  if constexpr (F == INT8) {
+  if constexpr (F == BF16) {  // the values themselves (x holds bf16 values exactly)
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = (__float_as_uint(x[2 * i]) >> 16) | (__float_as_uint(x[2 * i + 1]) & 0xFFFF0000u);
+    if (active)
+      *reinterpret_cast<uint4*>(cache + row * (2 * D) + sub * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if constexpr (F == INT8) {
     uint32_t w[2] = {0u, 0u};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {

@@ -170,6 +170,7 @@ cudaError_t dispatch_write_d(const WriteArgs& a, int kf, int vf, bool kvarn, cud
   KVQ_W(E5M2, INT8, false)
   KVQ_W(E5M2, E4M3, false)
   KVQ_W(E5M2, E5M2, false)
+  KVQ_W(BF16, BF16, false)
 #undef KVQ_W
   return cudaErrorNotSupported;
 }

@@ -18,7 +18,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
-FMT = {"int8": 1, "fp8_e4m3": 2, "fp8_e5m2": 3, "int4_asym": 4, "uint8_asym": 5}
+FMT = {"int8": 1, "fp8_e4m3": 2, "fp8_e5m2": 3, "int4_asym": 4, "uint8_asym": 5, "bf16": 6}
 FLAG_VARNORM_ROTATE = 1
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARGUMENT", 2: "KVQ_ERR_UNSUPPORTED",
           3: "KVQ_ERR_WORKSPACE", 4: "KVQ_ERR_CUDA"}
@@ -143,7 +143,7 @@ class KVCache:
 
 
 def row_bytes(fmt: str, head_dim: int) -> int:
-    return head_dim // 2 if fmt == "int4_asym" else head_dim
+    return head_dim // 2 if fmt == "int4_asym" else 2 * head_dim if fmt == "bf16" else head_dim
 
 
 def meta_fields(fmt: str, varnorm_rotate: bool) -> int:

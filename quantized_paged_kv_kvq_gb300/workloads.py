@@ -219,6 +219,11 @@ WORKLOADS = {
                          block_size=16, ctx_lo=512, ctx_hi=8192, k_fmt="fp8_e5m2",
                          v_fmt="fp8_e5m2", k_scale_rule="1.0", v_scale_rule="1.0",
                          k_outliers=(4, 10.0)),
+    # the same Llama-3-8B shape and inputs with the unquantized 16-bit cache
+    # (the --kv-cache-dtype auto baseline every quantized format is compared with)
+    "llama8b_bf16": dict(num_seqs=64, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                         ctx_lo=256, ctx_hi=4096, k_fmt="bf16", v_fmt="bf16",
+                         k_scale_rule=None, v_scale_rule=None, k_outliers=(4, 10.0)),
     # Llama-3-70B-shaped INT4 asymmetric decode layer (GQA 8)
     "llama70b_int4": dict(num_seqs=32, num_q_heads=64, num_kv_heads=8, head_dim=128,
                           block_size=16, ctx_lo=8192, ctx_hi=32768, k_fmt="int4_asym",
@@ -231,7 +236,7 @@ WORKLOADS = {
                        k_outliers=(4, 10.0), token_magnitude_sigma=0.5),
 }
 
-SEEDS = {"tiny_int8": 1001, "llama8b_int8": 1002, "llama8b_e4m3k_int8v": 1003,
+SEEDS = {"tiny_int8": 1001, "llama8b_int8": 1002, "llama8b_bf16": 1002, "llama8b_e4m3k_int8v": 1003,
          "llama8b_e5m2": 1013, "llama70b_int4": 1004, "kvarn_131k": 1005}
 
 

@@ -171,3 +171,15 @@ def test_wait_hook_validation(lib):
     assert lib.kvq_debug_arm_wait_timeout(-5, 0, 0) == 1
     assert lib.kvq_debug_arm_wait_timeout(100, -2, 0) == 1
     assert lib.kvq_debug_arm_wait_timeout(100, 0, -3) == 1
+
+
+def test_bf16_cache_validation(lib):
+    """The 16-bit cache is K and V both (one decode family), takes no scale,
+    no per-head scales and no rotation."""
+    assert _write(lib, _desc(k_fmt=6, v_fmt=6, k_scale=0.0, v_scale=float("nan")), n=0) == 0
+    assert _write(lib, _desc(k_fmt=6, v_fmt=1)) == 2
+    assert _write(lib, _desc(k_fmt=1, v_fmt=6)) == 2
+    assert _write(lib, _desc(k_fmt=6, v_fmt=4, v_meta=FAKE)) == 2
+    assert _write(lib, _desc(k_fmt=6, v_fmt=6, flags=1)) == 2
+    assert _write(lib, _desc(k_fmt=6, v_fmt=6, k_head_scales=FAKE)) == 1
+    assert _write(lib, _desc(k_fmt=7, v_fmt=7)) == 1

@@ -27,6 +27,7 @@ SMALL = {
     "llama8b_e5m2": dict(num_seqs=6, ctx_lo=1, ctx_hi=700),
     "llama70b_int4": dict(num_seqs=4, ctx_lo=1, ctx_hi=900),
     "kvarn_131k": dict(num_seqs=3, ctx_lo=1, ctx_hi=900),
+    "llama8b_bf16": dict(num_seqs=6, ctx_lo=1, ctx_hi=700),
 }
 
 

@@ -17,6 +17,7 @@ SMALL = {
     "llama8b_e5m2": dict(num_seqs=6, ctx_lo=1, ctx_hi=700),
     "llama70b_int4": dict(num_seqs=4, ctx_lo=1, ctx_hi=900),
     "kvarn_131k": dict(num_seqs=3, ctx_lo=1, ctx_hi=900),
+    "llama8b_bf16": dict(num_seqs=6, ctx_lo=1, ctx_hi=700),
 }
 
 
@@ -32,7 +33,7 @@ def test_decode_matches_oracle(name):
 
 
 @pytest.mark.parametrize("name", ["llama8b_int8", "llama70b_int4", "kvarn_131k",
-                                  "llama8b_e4m3k_int8v"])
+                                  "llama8b_e4m3k_int8v", "llama8b_bf16"])
 @pytest.mark.parametrize("ctas", [1, 3, 7, 64, 0])
 def test_split_invariance(name, ctas):
     """1, 3, 7, 64 stream-K ranges (and the automatic count) agree with the
@@ -60,7 +61,7 @@ def test_long_sequence_merges_in_two_levels(name, ctas):
 
 
 @pytest.mark.parametrize("name", ["llama8b_int8", "llama70b_int4", "kvarn_131k", "tiny_int8",
-                                  "llama8b_e5m2"])
+                                  "llama8b_e5m2", "llama8b_bf16"])
 def test_context_length_edge_cases(name):
     bs = W.WORKLOADS[name]["block_size"]
     lens = np.array([0, 1, bs - 1, bs, bs + 1, 15, 16, 17, 63, 64, 65, 0, 2 * bs + 3], np.int32)
@@ -91,7 +92,7 @@ def test_block_permutation_gives_identical_output():
     assert torch.equal(out1, out2)
 
 
-@pytest.mark.parametrize("name", ["llama8b_int8", "kvarn_131k", "llama70b_int4"])
+@pytest.mark.parametrize("name", ["llama8b_int8", "kvarn_131k", "llama70b_int4", "llama8b_bf16"])
 def test_block_sizes_agree(name):
     """Pages of 8, 16, 32, 64 and 128 tokens: codes bit-exact with the oracle's
     cache of the same page size, outputs within tolerance and alike."""
@@ -119,6 +120,8 @@ SMALL_PAGE_SHAPES = {
     "int4_d64_2heads": ("llama70b_int4", dict(num_q_heads=8, num_kv_heads=2, head_dim=64)),
     "kvarn_d128_2heads": ("kvarn_131k", dict(num_q_heads=8, num_kv_heads=2)),
     "fp8_d128_4heads": ("llama8b_e4m3k_int8v", dict(num_q_heads=16, num_kv_heads=4)),
+    "bf16_d128_2heads": ("llama8b_bf16", dict(num_q_heads=8, num_kv_heads=2)),
+    "bf16_d64_2heads": ("llama8b_bf16", dict(num_q_heads=8, num_kv_heads=2, head_dim=64)),
 }
 
 
@@ -167,7 +170,7 @@ def test_decode_is_deterministic():
 
 
 @pytest.mark.parametrize("name", ["llama8b_int8", "llama8b_e4m3k_int8v", "llama8b_e5m2",
-                                  "llama70b_int4", "kvarn_131k"])
+                                  "llama70b_int4", "kvarn_131k", "llama8b_bf16"])
 def test_decode_full_size_sampled(name):
     """The full-size workload, written and decoded in the launch configuration
     the benchmark times; a sample of (sequence, kv-head) pairs is computed by
