@@ -33,9 +33,8 @@ sys.path.insert(0, ROOT)
 DEFAULT_WORKLOAD = "llama8b_int8"
 METRIC = "quantized paged decode: effective KV GB/s vs HBM peak; decode & cache-write tok/s"
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SOURCES = ["decode.cuh", "decode_launch.cuh", "kvq_device.cuh", "quant_row.cuh",
-                  "decode_d128_sym.cu", "decode_d128_asym.cu", "decode_d64_sym.cu",
-                  "decode_d64_asym.cu"]
+# the kernel's own code (the instance units only list template arguments)
+DECODE_SOURCES = ["decode.cuh", "decode_launch.cuh", "kvq_device.cuh", "quant_row.cuh"]
 WRITE_SOURCES = ["write.cu", "kvq_device.cuh", "quant_row.cuh"]
 WRITE_ASYM_SOURCES = ["write_asym.cu", "kvq_device.cuh", "quant_row.cuh"]
 

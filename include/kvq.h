@@ -243,6 +243,38 @@ kvq_status kvq_decode_append(const kvq_cache_desc* cache, void* k_cache, void* v
                              size_t workspace_bytes, kvq_stream_t stream);
 
 /*
+ * kvq_decode_mixed -- kvq_paged_decode_ex (new_key == NULL) or
+ * kvq_decode_append over a cache whose sequences use pages of different sizes
+ * (the variable page sizes that the KVarN article's section 'Perspective'
+ * looks ahead to).
+ *
+ * Each page class is a pool of pages of one size: classes[c] describes it
+ * (block_size 16, 32, 64 or 128 and num_blocks of its own, its own metadata
+ * arrays; formats, num_kv_heads, head_dim, flags, scales, per-head scales and
+ * signs equal to class 0's), with codes k_caches[c] / v_caches[c] (host
+ * arrays of device pointers).  num_classes: 1 or 2.
+ * seq_class: device uint8 [num_seqs], the class of each sequence; row s of
+ *   block_table holds block ids of that class's pool, and max_blocks_per_seq
+ *   must cover max_context_len at the smallest page size.  A class id outside
+ *   [0, num_classes) sets KVQ_DEVERR_CLASS_RANGE and reads class 0.
+ * Writes go through kvq_write_cache with each class's description, codes and
+ *   slots (slot = block * class block_size + offset).
+ * new_key, new_value, key_stride, value_stride: as in kvq_decode_append (the
+ *   new row lands in the sequence's class), or NULL for a plain decode.
+ * Everything else (workspace and its size, num_ctas, output) is that of
+ * kvq_paged_decode_ex / kvq_decode_append for class 0's description.
+ */
+kvq_status kvq_decode_mixed(const kvq_cache_desc* classes, int32_t num_classes,
+                            void* const* k_caches, void* const* v_caches,
+                            const uint8_t* seq_class, const void* new_key, const void* new_value,
+                            int64_t key_stride, int64_t value_stride, void* out,
+                            const void* query, int32_t num_seqs, int32_t num_q_heads,
+                            const int32_t* block_table, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, int32_t max_context_len,
+                            float sm_scale, int32_t num_ctas, void* workspace,
+                            size_t workspace_bytes, kvq_stream_t stream);
+
+/*
  * kvq_paged_decode_static -- kvq_paged_decode_ex for callers that cannot
  * allocate device memory.  None of the source pages has a counterpart of
  * this entry point: it exists for integration, not for the method.
@@ -326,6 +358,7 @@ kvq_status kvq_calibrate_head_scales(const void* x, int64_t num_tokens, int32_t 
 #define KVQ_DEVERR_COMBINE 8u       /* a split-sequence merge counter update gave up */
 #define KVQ_DEVERR_TIMEOUT 16u      /* a pipeline barrier wait gave up: the CTA stopped
                                        early, the launch's results are invalid */
+#define KVQ_DEVERR_CLASS_RANGE 32u  /* a page class id outside the call's classes */
 
 /*
  * kvq_debug_arm_wait_timeout -- test hook for the decode kernel's bounded

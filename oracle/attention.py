@@ -62,6 +62,25 @@ def paged_decode(query, k_codes, k_meta, v_codes, v_meta, block_table, context_l
     return out
 
 
+def paged_decode_classes(query, classes, seq_class, block_table, context_lens, k_fmt, v_fmt,
+                         k_scale, v_scale, sm_scale, kvarn=False, signs=None) -> np.ndarray:
+    """paged_decode over a cache of several page classes (the KVarN article's
+    variable page sizes, section 'Perspective'): classes[c] = (k codes, k meta,
+    v codes, v meta, block size) of pool c; sequence s reads pool
+    seq_class[s] through its row of the block table.  Each sequence's attention
+    is the plain definition over its own tokens, whatever its page size."""
+    query = np.asarray(query, np.float64)
+    s_count, hq, d = query.shape
+    out = np.zeros((s_count, hq, d))
+    for c, (kc, km, vc, vm, bs) in enumerate(classes):
+        pairs = [(s, h) for s in range(s_count) if int(seq_class[s]) == c
+                 for h in range(kc.shape[2])]
+        if pairs:
+            out += paged_decode(query, kc, km, vc, vm, block_table, context_lens, bs, k_fmt,
+                                v_fmt, k_scale, v_scale, sm_scale, kvarn, signs, pairs=pairs)
+    return out
+
+
 def default_sm_scale(head_dim: int) -> np.float32:
     """float32(1/sqrt(D)), the usual attention scale."""
     return np.float32(1.0 / np.sqrt(np.float64(head_dim)))

@@ -242,22 +242,53 @@ struct AppendRows {
   int64_t value_stride = 0;
 };
 
-kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const void* v_cache,
+// Page classes of a mixed cache: every class the same formats, kv-heads,
+// head_dim, flags, scales and signs as class 0; pages of 16 tokens or more
+// (an 8-token page takes its own kernel instance, one page size per call).
+kvq_status check_classes(const kvq_cache_desc* classes, int32_t num_classes,
+                         void* const* k_caches, void* const* v_caches, const uint8_t* seq_class) {
+  if (classes == nullptr || k_caches == nullptr || v_caches == nullptr || seq_class == nullptr)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_classes < 1 || num_classes > kMaxPageClasses) return KVQ_ERR_UNSUPPORTED;
+  const kvq_cache_desc& c0 = classes[0];
+  for (int c = 0; c < num_classes; ++c) {
+    const kvq_cache_desc& x = classes[c];
+    kvq_status st = check_cache(&x);
+    if (st != KVQ_OK) return st;
+    if (x.k_fmt != c0.k_fmt || x.v_fmt != c0.v_fmt || x.num_kv_heads != c0.num_kv_heads ||
+        x.head_dim != c0.head_dim || x.flags != c0.flags || x.signs != c0.signs ||
+        x.k_head_scales != c0.k_head_scales || x.v_head_scales != c0.v_head_scales ||
+        (scaled(x.k_fmt) && x.k_scale != c0.k_scale) || (scaled(x.v_fmt) && x.v_scale != c0.v_scale))
+      return KVQ_ERR_INVALID_ARGUMENT;
+    if (x.block_size < 16) return KVQ_ERR_UNSUPPORTED;
+    if (k_caches[c] == nullptr || v_caches[c] == nullptr || !aligned(k_caches[c], 16) ||
+        !aligned(v_caches[c], 16))
+      return KVQ_ERR_INVALID_ARGUMENT;
+  }
+  return KVQ_OK;
+}
+
+kvq_status decode_call(const kvq_cache_desc* classes, int32_t num_classes,
+                       void* const* k_caches, void* const* v_caches, const uint8_t* seq_class,
                        void* out, const void* query, int32_t num_seqs, int32_t num_q_heads,
                        const int32_t* block_table, int32_t max_blocks_per_seq,
                        const int32_t* context_lens, int32_t max_context_len, float sm_scale,
                        int32_t num_ctas, void* workspace, size_t workspace_bytes,
                        const AppendRows& app, kvq_stream_t stream) {
+  const kvq_cache_desc* cache = classes;  // class 0: formats, heads, scales of every class
   int NC = 0;
   kvq_status st = decode_shape(cache, num_seqs, num_q_heads, max_context_len, num_ctas, &NC);
   if (st != KVQ_OK) return st;
   if (num_seqs == 0) return KVQ_OK;
-  if (!k_cache || !v_cache || !out || !query || !block_table || !context_lens)
+  if (!k_caches[0] || !v_caches[0] || !out || !query || !block_table || !context_lens)
     return KVQ_ERR_INVALID_ARGUMENT;
-  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) || !aligned(query, 16) ||
-      !aligned(block_table, 4) || !aligned(context_lens, 4))
+  if (!aligned(k_caches[0], 16) || !aligned(v_caches[0], 16) || !aligned(out, 16) ||
+      !aligned(query, 16) || !aligned(block_table, 4) || !aligned(context_lens, 4))
     return KVQ_ERR_INVALID_ARGUMENT;
-  if (max_blocks_per_seq < ceil_div(max_context_len, cache->block_size) || max_blocks_per_seq < 0)
+  int min_bs = cache->block_size;
+  for (int c = 1; c < num_classes; ++c)
+    min_bs = classes[c].block_size < min_bs ? classes[c].block_size : min_bs;
+  if (max_blocks_per_seq < ceil_div(max_context_len, min_bs) || max_blocks_per_seq < 0)
     return KVQ_ERR_INVALID_ARGUMENT;
   if (!isfinite(sm_scale)) return KVQ_ERR_INVALID_ARGUMENT;
   const size_t need =
@@ -266,10 +297,23 @@ kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const v
   if (need > 0 && !aligned(workspace, 16)) return KVQ_ERR_INVALID_ARGUMENT;
   const bool kvarn = (cache->flags & KVQ_FLAG_VARNORM_ROTATE) != 0;
   DecodeArgs a;
-  a.k_cache = static_cast<const uint8_t*>(k_cache);
-  a.v_cache = static_cast<const uint8_t*>(v_cache);
-  a.k_meta = static_cast<const __half*>(cache->k_meta);
-  a.v_meta = static_cast<const __half*>(cache->v_meta);
+  const bool append = app.key != nullptr;
+  for (int c = 0; c < kMaxPageClasses; ++c) {
+    const int cc = c < num_classes ? c : 0;
+    const kvq_cache_desc& x = classes[cc];
+    a.k_cache[c] = static_cast<const uint8_t*>(k_caches[cc]);
+    a.v_cache[c] = static_cast<const uint8_t*>(v_caches[cc]);
+    a.k_meta[c] = static_cast<const __half*>(x.k_meta);
+    a.v_meta[c] = static_cast<const __half*>(x.v_meta);
+    a.block_shift[c] = __builtin_ctz(static_cast<unsigned>(x.block_size));
+    a.num_blocks[c] = x.num_blocks;
+    a.k_cache_w[c] = append ? static_cast<uint8_t*>(k_caches[cc]) : nullptr;
+    a.v_cache_w[c] = append ? static_cast<uint8_t*>(v_caches[cc]) : nullptr;
+    a.k_meta_w[c] = append ? static_cast<__half*>(x.k_meta) : nullptr;
+    a.v_meta_w[c] = append ? static_cast<__half*>(x.v_meta) : nullptr;
+  }
+  a.seq_class = seq_class;
+  a.num_classes = num_classes;
   a.query = static_cast<const uint16_t*>(query);
   a.out = static_cast<uint16_t*>(out);
   a.block_table = block_table;
@@ -291,9 +335,6 @@ kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const v
   a.num_kv_heads = cache->num_kv_heads;
   a.gqa = num_q_heads / cache->num_kv_heads;
   a.heads_per_cta = heads_per_cta(cache->num_kv_heads);
-  a.block_size = cache->block_size;
-  a.block_shift = __builtin_ctz(static_cast<unsigned>(cache->block_size));
-  a.num_blocks = cache->num_blocks;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.max_context_len = max_context_len;
   a.num_ctas = NC;
@@ -307,11 +348,6 @@ kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const v
   a.new_value = static_cast<const uint16_t*>(app.value);
   a.new_key_stride = app.key_stride;
   a.new_value_stride = app.value_stride;
-  const bool append = app.key != nullptr;
-  a.k_cache_w = append ? static_cast<uint8_t*>(const_cast<void*>(k_cache)) : nullptr;
-  a.v_cache_w = append ? static_cast<uint8_t*>(const_cast<void*>(v_cache)) : nullptr;
-  a.k_meta_w = append ? static_cast<__half*>(cache->k_meta) : nullptr;
-  a.v_meta_w = append ? static_cast<__half*>(cache->v_meta) : nullptr;
   volatile float one = 1.0f;  // 1/scale, one IEEE float32 division, as kvq_write_cache
   a.k_inv = scaled(cache->k_fmt) ? one / cache->k_scale : 1.0f;
   a.v_inv = scaled(cache->v_fmt) ? one / cache->v_scale : 1.0f;
@@ -323,19 +359,38 @@ kvq_status decode_call(const kvq_cache_desc* cache, const void* k_cache, const v
     a.withhold_cta = g_wait_hook_cta.load();
     a.withhold_tile = g_wait_hook_tile.load();
   }
-  cudaError_t e;
+  cudaError_t e = cudaErrorNotSupported;
   const int kf = cache->k_fmt, vf = cache->v_fmt;
-  if (kf == KVQ_FMT_BF16) {
-    e = launch_decode_bf16(a, cache->head_dim, stream);
-  } else if (is_asym(kf)) {
-    e = cache->head_dim == 64 ? launch_decode_d64_asym(a, kf, vf, kvarn, stream)
-                              : launch_decode_d128_asym(a, kf, vf, kvarn, stream);
-  } else {
-    e = cache->head_dim == 64 ? launch_decode_d64_sym(a, kf, vf, stream)
-                              : launch_decode_d128_sym(a, kf, vf, stream);
+#define KVQ_UNIT_LAUNCHER(U) launch_##U,
+  static const DecodeLauncher launchers[] = {KVQ_DECODE_UNITS(KVQ_UNIT_LAUNCHER)};
+#undef KVQ_UNIT_LAUNCHER
+  for (DecodeLauncher f : launchers) {  // the unit that holds the instance launches it
+    e = f(a, cache->head_dim, kf, vf, kvarn, stream);
+    if (e != cudaErrorNotSupported) break;
   }
   if (e == cudaErrorNotSupported) return KVQ_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+// The new-token rows of kvq_decode_append, checked.
+kvq_status append_rows(const kvq_cache_desc* cache, int32_t num_seqs, const void* new_key,
+                       const void* new_value, int64_t key_stride, int64_t value_stride,
+                       AppendRows* app) {
+  if (num_seqs > 0) {
+    if (!new_key || !new_value || !aligned(new_key, 16) || !aligned(new_value, 16))
+      return KVQ_ERR_INVALID_ARGUMENT;
+    const int64_t row = static_cast<int64_t>(cache->num_kv_heads) * cache->head_dim;
+    if (key_stride < row || value_stride < row || key_stride % 8 || value_stride % 8)
+      return KVQ_ERR_INVALID_ARGUMENT;
+    if (!write_supported(cache->k_fmt, cache->v_fmt,
+                         (cache->flags & KVQ_FLAG_VARNORM_ROTATE) != 0))
+      return KVQ_ERR_UNSUPPORTED;
+  }
+  app->key = new_key;
+  app->value = new_value;
+  app->key_stride = key_stride;
+  app->value_stride = value_stride;
+  return KVQ_OK;
 }
 
 }  // namespace
@@ -348,7 +403,9 @@ kvq_status kvq_paged_decode_ex(const kvq_cache_desc* cache, const void* k_cache,
                                int32_t max_blocks_per_seq, const int32_t* context_lens,
                                int32_t max_context_len, float sm_scale, int32_t num_ctas,
                                void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
-  return decode_call(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
+  void* kc = const_cast<void*>(k_cache);
+  void* vc = const_cast<void*>(v_cache);
+  return decode_call(cache, 1, &kc, &vc, nullptr, out, query, num_seqs, num_q_heads, block_table,
                      max_blocks_per_seq, context_lens, max_context_len, sm_scale, num_ctas,
                      workspace, workspace_bytes, AppendRows{}, stream);
 }
@@ -362,24 +419,34 @@ kvq_status kvq_decode_append(const kvq_cache_desc* cache, void* k_cache, void* v
                              void* workspace, size_t workspace_bytes, kvq_stream_t stream) {
   kvq_status st = check_cache(cache);
   if (st != KVQ_OK) return st;
-  if (num_seqs > 0) {
-    if (!new_key || !new_value || !aligned(new_key, 16) || !aligned(new_value, 16))
-      return KVQ_ERR_INVALID_ARGUMENT;
-    const int64_t row = static_cast<int64_t>(cache->num_kv_heads) * cache->head_dim;
-    if (key_stride < row || value_stride < row || key_stride % 8 || value_stride % 8)
-      return KVQ_ERR_INVALID_ARGUMENT;
-    if (!write_supported(cache->k_fmt, cache->v_fmt,
-                         (cache->flags & KVQ_FLAG_VARNORM_ROTATE) != 0))
-      return KVQ_ERR_UNSUPPORTED;
-  }
   AppendRows app;
-  app.key = new_key;
-  app.value = new_value;
-  app.key_stride = key_stride;
-  app.value_stride = value_stride;
-  return decode_call(cache, k_cache, v_cache, out, query, num_seqs, num_q_heads, block_table,
-                     max_blocks_per_seq, context_lens, max_context_len, sm_scale, num_ctas,
-                     workspace, workspace_bytes, app, stream);
+  st = append_rows(cache, num_seqs, new_key, new_value, key_stride, value_stride, &app);
+  if (st != KVQ_OK) return st;
+  return decode_call(cache, 1, &k_cache, &v_cache, nullptr, out, query, num_seqs, num_q_heads,
+                     block_table, max_blocks_per_seq, context_lens, max_context_len, sm_scale,
+                     num_ctas, workspace, workspace_bytes, app, stream);
+}
+
+kvq_status kvq_decode_mixed(const kvq_cache_desc* classes, int32_t num_classes,
+                            void* const* k_caches, void* const* v_caches,
+                            const uint8_t* seq_class, const void* new_key, const void* new_value,
+                            int64_t key_stride, int64_t value_stride, void* out,
+                            const void* query, int32_t num_seqs, int32_t num_q_heads,
+                            const int32_t* block_table, int32_t max_blocks_per_seq,
+                            const int32_t* context_lens, int32_t max_context_len,
+                            float sm_scale, int32_t num_ctas, void* workspace,
+                            size_t workspace_bytes, kvq_stream_t stream) {
+  kvq_status st = check_classes(classes, num_classes, k_caches, v_caches, seq_class);
+  if (st != KVQ_OK) return st;
+  AppendRows app;
+  if (new_key != nullptr || new_value != nullptr) {
+    st = append_rows(classes, num_seqs, new_key, new_value, key_stride, value_stride, &app);
+    if (st != KVQ_OK) return st;
+  }
+  return decode_call(classes, num_classes, k_caches, v_caches, seq_class, out, query, num_seqs,
+                     num_q_heads, block_table, max_blocks_per_seq, context_lens,
+                     max_context_len, sm_scale, num_ctas, workspace, workspace_bytes, app,
+                     stream);
 }
 
 kvq_status kvq_paged_decode(const kvq_cache_desc* cache, const void* k_cache,
@@ -449,12 +516,10 @@ kvq_status kvq_get_device_error(kvq_stream_t stream, uint32_t* bits) {
   if (bits == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return KVQ_ERR_CUDA;
   unsigned v = 0;
+#define KVQ_UNIT_TAKE(U) take_error_bits_##U,
   cudaError_t (*take[])(unsigned*) = {take_error_bits_write, take_error_bits_write_asym,
-                                      take_error_bits_decode_d64_sym,
-                                      take_error_bits_decode_d128_sym,
-                                      take_error_bits_decode_d64_asym,
-                                      take_error_bits_decode_d128_asym,
-                                      take_error_bits_decode_bf16};
+                                      KVQ_DECODE_UNITS(KVQ_UNIT_TAKE)};
+#undef KVQ_UNIT_TAKE
   for (auto f : take)
     if (f(&v) != cudaSuccess) return KVQ_ERR_CUDA;
   *bits = v;

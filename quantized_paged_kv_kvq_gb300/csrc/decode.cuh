@@ -403,6 +403,11 @@ __device__ __forceinline__ uint32_t pack_op2(float lo, float hi) {
   return BF ? pack_bf162(lo, hi) : pack_half2(lo, hi);
 }
 
+// Page modes of the decode kernel (its PAGES template argument).
+constexpr int kPagesOne = 0;    // one pool, pages of 16 tokens or more
+constexpr int kPages8 = 1;      // one pool of 8-token pages
+constexpr int kPagesMixed = 2;  // a pool per page class, pages of 16 tokens or more
+
 // The producer's position in the range.
 struct Cursor {
   long long ps;  // global index of the first tile of sequence s
@@ -411,13 +416,28 @@ struct Cursor {
   int blk;         // block id of that tile (read ahead)
   int nx, nx_ctx;  // next sequence of the range with tokens (num_seqs: none)
   int i;           // loads issued
+  int cls;         // page class of sequence s
 };
 
-static_assert(sizeof(Cursor) <= 40, "the cursor lives in scratch words 16..20");
+static_assert(sizeof(Cursor) <= 48, "the cursor lives in scratch words 16..21");
 
+// Tensor maps of each page class's codes and metadata (N classes).
+template <int N>
 struct DecodeMaps {
-  CUtensorMap k, v, km, vm;
+  CUtensorMap k[N], v[N], km[N], vm[N];
 };
+template <int PAGES>
+using DecodeMapsOf = DecodeMaps<PAGES == kPagesMixed ? kMaxPageClasses : 1>;
+
+// Page class of sequence s (0 without a class array; a class outside the
+// call's raises KVQ_DEVERR_CLASS_RANGE and reads class 0).
+__device__ __forceinline__ int seq_class_of(const DecodeArgs& a, int s) {
+  if (a.seq_class == nullptr) return 0;
+  const int c = a.seq_class[s];
+  if (c < a.num_classes) return c;
+  raise_error(32u);  // KVQ_DEVERR_CLASS_RANGE
+  return 0;
+}
 
 // One stage's tile: which sequence / tile it is and how it ends a segment.
 struct TileHeader {
@@ -650,7 +670,8 @@ __device__ __forceinline__ void merge_slots(const DecodeArgs& a, int s, long lon
 // to this range alone, so no other CTA reads the new row.  The warps walk the
 // sequences from the range's first one, 32 at a time (a lane per sequence,
 // prefix sum of tile counts, ballot of those that end inside the range).
-template <int D, int KF, int VF, bool KVARN>
+// MIXED: the row lands in the pool of the sequence's page class.
+template <int D, int KF, int VF, bool KVARN, bool MIXED>
 __device__ __forceinline__ void append_new_tokens(const DecodeArgs& a, long long R0, long long R1,
                                                int s0, long long ps0, int h, int lane) {
   constexpr int LPR = RowGeom<D>::LPR;
@@ -688,22 +709,24 @@ __device__ __forceinline__ void append_new_tokens(const DecodeArgs& a, long long
       mine &= mine - 1u;
       const int sq = base + src;
       const int pos = __shfl_sync(0xffffffffu, cc, src) - 1;
-      const int blk = a.block_table[static_cast<size_t>(sq) * a.max_blocks_per_seq + (pos >> a.block_shift)];
-      if (blk < 0 || blk >= a.num_blocks) {
+      const int cls = MIXED ? seq_class_of(a, sq) : 0;
+      const int bshift = a.block_shift[cls], bsz = 1 << bshift;
+      const int blk = a.block_table[static_cast<size_t>(sq) * a.max_blocks_per_seq + (pos >> bshift)];
+      if (blk < 0 || blk >= a.num_blocks[cls]) {
         if (lane == 0) raise_error(2u);  // KVQ_DEVERR_BLOCK_RANGE: nothing written
         continue;
       }
-      const int off = pos & (a.block_size - 1);
-      const size_t row = (static_cast<size_t>(blk) * a.block_size + off) * Hkv + h;
+      const int off = pos & (bsz - 1);
+      const size_t row = (static_cast<size_t>(blk) * bsz + off) * Hkv + h;
       float x[8];
       unpack8(*reinterpret_cast<const uint4*>(a.new_key + static_cast<size_t>(sq) * a.new_key_stride +
                                               static_cast<size_t>(h) * D + sub * 8), x);
-      quantize_store<D, KF, KVARN>(x, lane < LPR, h, sub, row, a.k_cache_w, a.k_meta_w, kinv, blk,
-                                   off, Hkv, a.block_size, sign_bits, a.cR);
+      quantize_store<D, KF, KVARN>(x, lane < LPR, h, sub, row, a.k_cache_w[cls], a.k_meta_w[cls],
+                                   kinv, blk, off, Hkv, bsz, sign_bits, a.cR);
       unpack8(*reinterpret_cast<const uint4*>(a.new_value + static_cast<size_t>(sq) * a.new_value_stride +
                                               static_cast<size_t>(h) * D + sub * 8), x);
-      quantize_store<D, VF, KVARN>(x, lane < LPR, h, sub, row, a.v_cache_w, a.v_meta_w, vinv, blk,
-                                   off, Hkv, a.block_size, sign_bits, a.cR);
+      quantize_store<D, VF, KVARN>(x, lane < LPR, h, sub, row, a.v_cache_w[cls], a.v_meta_w[cls],
+                                   vinv, blk, off, Hkv, bsz, sign_bits, a.cR);
     }
     ps += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -718,11 +741,13 @@ __device__ __forceinline__ void append_new_tokens(const DecodeArgs& a, long long
 // range of such a sequence merges the slots.  Store-then-fence-then-load of
 // the tags guarantees at least one finder; a claim word per sequence keeps it
 // to one.
-// SPLIT: pages of 8 tokens (a tile is two pages); a separate instance, so that
-// the other page sizes keep the one-box path's registers.
-template <int D, int KF, int VF, bool KVARN, bool SPLIT>
+// PAGES: kPagesOne (one pool, pages of 16 tokens or more), kPages8 (8-token
+// pages: a tile is two pages) or kPagesMixed (each sequence in the pool of its
+// page class); separate instances, so that one page size keeps the one-box
+// path's registers.
+template <int D, int KF, int VF, bool KVARN, int PAGES>
 __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
-    decode_partition_kernel(const DecodeArgs a, const __grid_constant__ DecodeMaps maps) {
+    decode_partition_kernel(const DecodeArgs a, const __grid_constant__ DecodeMapsOf<PAGES> maps) {
   using C = DecodeCfg<D, KF, VF, KVARN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -741,7 +766,8 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
   const int m_off = v_off + C::align(hpc * C::V_HEAD);  // K metadata box, then V's
   const int vm_off = m_off + C::meta_room(hpc, C::KMF);
   // 8-token pages: a 16-token tile is two pages, loaded as two boxes each
-  constexpr bool split = SPLIT;
+  constexpr bool split = PAGES == kPages8;
+  constexpr bool mixed = PAGES == kPagesMixed;
   const uint32_t ring_end = C::STAGES * stage_bytes;
   const int qrb = q_rows_bytes(G, D);
   const uint32_t qbuf_s = base_s + ring_end + warp * qrb;  // this warp's query rows (bf16)
@@ -754,11 +780,11 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
       reinterpret_cast<long long*>(smem + hdr_off + C::STAGES * (sizeof(TileHeader) + 16));
   // scratch: [0] T, [1] first sequence, [2] its first tile, [3] R1, [4..12) scan,
   // [12..16) partial segments: (first tile, sequence << 32 | tiles) per end of the range,
-  // [16..21) producer cursor, [21] second page id, [22] abort flag (int),
-  // [23] withheld tile (int; test hook), [24] per end of the range: warps whose
+  // [16..22) producer cursor, [22] second page id, [23] abort flag (int),
+  // [24] withheld tile (int; test hook), [25] per end of the range: warps whose
   // rows of the partial slot are stored (two ints)
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(scratch + 22);
-  int* const done_warps = reinterpret_cast<int*>(scratch + 24);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(scratch + 23);
+  int* const done_warps = reinterpret_cast<int*>(scratch + 25);
   const int spin = a.spin_limit;
 
   // this warp's G query rows of sequence s -> shared memory (asynchronous)
@@ -848,7 +874,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
   const long long ps_first = scratch[2];
   prefetch_q(s_first);
   if (a.new_key != nullptr) {  // new-token append: codes stored before any tile is loaded
-    append_new_tokens<D, KF, VF, KVARN>(a, R0, R1, s_first, ps_first, h, lane);
+    append_new_tokens<D, KF, VF, KVARN, mixed>(a, R0, R1, s_first, ps_first, h, lane);
     // the stores (generic proxy) before the tensor loads (async proxy) the
     // barrier below lets thread 0 issue
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -863,7 +889,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
     }
     for (int i = 12; i < 16; ++i) scratch[i] = -1;
     *abort_flag = 0;
-    reinterpret_cast<int*>(scratch + 23)[0] =
+    reinterpret_cast<int*>(scratch + 24)[0] =
         (k == a.withhold_cta && hg == 0) ? a.withhold_tile : -1;
     done_warps[0] = done_warps[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -873,22 +899,22 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
 
   // ---- producer cursor (thread 0): walks the range tile by tile
   const uint32_t tile_bytes = hpc * (C::K_HEAD + C::V_HEAD) + hpc * (C::KMF + C::VMF) * 32;
-  const int bs_shift = a.block_shift, bs_mask = a.block_size - 1;
   // The cursor lives in shared memory: only thread 0 uses it, and registers
   // held by every thread for it would be taken from the consumers.
   Cursor* cur = reinterpret_cast<Cursor*>(scratch + 16);
   // 8-token pages: block id of the cursor tile's second page (read ahead); kept
   // out of the cursor, whose copies stay as small as for the other page sizes
-  int* const cur_blk2 = reinterpret_cast<int*>(scratch + 21);
-  auto block_of = [&](const Cursor& u) {  // block id of the cursor's tile
-    return a.block_table[static_cast<size_t>(u.s) * a.max_blocks_per_seq + ((16 * u.t) >> bs_shift)];
+  int* const cur_blk2 = reinterpret_cast<int*>(scratch + 22);
+  auto block_of = [&](const Cursor& u) {  // block id of the cursor's tile (in its class's pool)
+    return a.block_table[static_cast<size_t>(u.s) * a.max_blocks_per_seq +
+                         ((16 * u.t) >> a.block_shift[mixed ? u.cls : 0])];
   };
   auto second_half = [&](const Cursor& u) {  // 8-token pages: tokens 8..15 of the tile exist
     return split && 16 * u.t + 8 < u.ctx;
   };
   auto block2_of = [&](const Cursor& u) {  // their page (entries past the context are never read)
     return second_half(u) ? a.block_table[static_cast<size_t>(u.s) * a.max_blocks_per_seq +
-                                          ((16 * u.t) >> bs_shift) + 1]
+                                          ((16 * u.t) >> a.block_shift[0]) + 1]
                           : 0;
   };
   auto find_next = [&](Cursor& u) {  // first sequence after u.s with tokens, if the range goes on
@@ -911,6 +937,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
     u.t = static_cast<int>(R0 - ps_first);
     u.ctx = min(a.context_lens[s_first], a.max_context_len);
     u.tiles = (u.ctx + 15) >> 4;
+    u.cls = mixed ? seq_class_of(a, u.s) : 0;
     u.blk = block_of(u);
     if constexpr (split) *cur_blk2 = block2_of(u);
     u.nx_ctx = 0;
@@ -931,21 +958,22 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
     hd.next_s = u.nx < S ? u.nx : -1;
     const int tok = 16 * u.t;
     int blk = u.blk;
-    if (blk < 0 || blk >= a.num_blocks) {
+    const int cl = mixed ? u.cls : 0;
+    if (blk < 0 || blk >= a.num_blocks[cl]) {
       raise_error(2u);  // KVQ_DEVERR_BLOCK_RANGE: read block 0 instead
       blk = 0;
     }
-    const int off = tok & bs_mask;
+    const int off = tok & ((1 << a.block_shift[cl]) - 1);
     const uint32_t sb = base_s + st * stage_bytes;
     const uint32_t bar = full_s + 8 * st;
     // test hook: this tile's loads are never issued (its stage never fills)
-    if (u.i == reinterpret_cast<const int*>(scratch + 23)[0]) {
+    if (u.i == reinterpret_cast<const int*>(scratch + 24)[0]) {
     } else if constexpr (split) {  // 8-token pages: the tile is two pages, each loaded as
       // per-head 8-row boxes (rows 0-7, then 8-15 of the head's [16][row] box)
       // and [head][field][8] metadata boxes (the second meta_half bytes on)
       const bool two = second_half(u);
       int blk2 = *cur_blk2;
-      if (two && (blk2 < 0 || blk2 >= a.num_blocks)) {
+      if (two && (blk2 < 0 || blk2 >= a.num_blocks[0])) {
         raise_error(2u);
         blk2 = 0;
       }
@@ -953,32 +981,35 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
       for (int hf = 0; hf < (two ? 2 : 1); ++hf) {
         const int b = hf ? blk2 : blk;
         for (int hh = 0; hh < hpc; ++hh) {
-          tma_codes_head<C::KB>(sb + hh * C::K_HEAD + hf * 8 * C::KB, &maps.k, hg * hpc + hh, 0, b,
-                                bar, pol);
-          tma_codes_head<C::VB>(sb + v_off + hh * C::V_HEAD + hf * 8 * C::VB, &maps.v,
+          tma_codes_head<C::KB>(sb + hh * C::K_HEAD + hf * 8 * C::KB, &maps.k[0], hg * hpc + hh, 0,
+                                b, bar, pol);
+          tma_codes_head<C::VB>(sb + v_off + hh * C::V_HEAD + hf * 8 * C::VB, &maps.v[0],
                                 hg * hpc + hh, 0, b, bar, pol);
         }
         if constexpr (C::KMF > 0)
-          tma_load_4d(sb + m_off + hf * C::meta_half(hpc, C::KMF), &maps.km, 0, 0, hg * hpc, b, bar,
-                      pol);
+          tma_load_4d(sb + m_off + hf * C::meta_half(hpc, C::KMF), &maps.km[0], 0, 0, hg * hpc, b,
+                      bar, pol);
         if constexpr (C::VMF > 0)
-          tma_load_4d(sb + vm_off + hf * C::meta_half(hpc, C::VMF), &maps.vm, 0, 0, hg * hpc, b,
+          tma_load_4d(sb + vm_off + hf * C::meta_half(hpc, C::VMF), &maps.vm[0], 0, 0, hg * hpc, b,
                       bar, pol);
       }
     } else {  // one box per tile (pages of 16 or more tokens)
       mbar_arrive_expect(bar, tile_bytes);
       if (a.one_box) {
-        tma_codes_heads<C::KB>(sb, &maps.k, off, hg * hpc, blk, bar, pol);
-        tma_codes_heads<C::VB>(sb + v_off, &maps.v, off, hg * hpc, blk, bar, pol);
+        tma_codes_heads<C::KB>(sb, &maps.k[cl], off, hg * hpc, blk, bar, pol);
+        tma_codes_heads<C::VB>(sb + v_off, &maps.v[cl], off, hg * hpc, blk, bar, pol);
       } else {
         for (int hh = 0; hh < hpc; ++hh) {
-          tma_codes_head<C::KB>(sb + hh * C::K_HEAD, &maps.k, hg * hpc + hh, off, blk, bar, pol);
-          tma_codes_head<C::VB>(sb + v_off + hh * C::V_HEAD, &maps.v, hg * hpc + hh, off, blk, bar,
+          tma_codes_head<C::KB>(sb + hh * C::K_HEAD, &maps.k[cl], hg * hpc + hh, off, blk, bar,
                                 pol);
+          tma_codes_head<C::VB>(sb + v_off + hh * C::V_HEAD, &maps.v[cl], hg * hpc + hh, off, blk,
+                                bar, pol);
         }
       }
-      if constexpr (C::KMF > 0) tma_load_4d(sb + m_off, &maps.km, off, 0, hg * hpc, blk, bar, pol);
-      if constexpr (C::VMF > 0) tma_load_4d(sb + vm_off, &maps.vm, off, 0, hg * hpc, blk, bar, pol);
+      if constexpr (C::KMF > 0)
+        tma_load_4d(sb + m_off, &maps.km[cl], off, 0, hg * hpc, blk, bar, pol);
+      if constexpr (C::VMF > 0)
+        tma_load_4d(sb + vm_off, &maps.vm[cl], off, 0, hg * hpc, blk, bar, pol);
     }
     ++u.i;
     if (++u.t == u.tiles && u.i < n) {  // on to the next sequence with tokens
@@ -992,6 +1023,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
       u.s = u.nx;
       u.ctx = u.nx_ctx;
       u.tiles = (u.ctx + 15) >> 4;
+      if constexpr (mixed) u.cls = seq_class_of(a, u.s);
       find_next(u);
     }
     if (u.i < n) {  // prefetched: consumed by the next issue
@@ -1397,7 +1429,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
     if (threadIdx.x == 0) {
       const int issued = cur->i;
       for (int t = issued > C::STAGES ? issued - C::STAGES : 0; t < issued; ++t) {
-        if (t == reinterpret_cast<const int*>(scratch + 23)[0]) continue;
+        if (t == reinterpret_cast<const int*>(scratch + 24)[0]) continue;
         mbar_wait(full_s + 8 * (t % C::STAGES), (t / C::STAGES) & 1, spin);
       }
     }

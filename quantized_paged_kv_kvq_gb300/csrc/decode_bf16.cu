@@ -8,7 +8,9 @@ namespace kvq {
 
 KVQ_ERROR_ACCESSOR(take_error_bits_decode_bf16)
 
-cudaError_t launch_decode_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st) {
+cudaError_t launch_decode_bf16(const DecodeArgs& a, int head_dim, int kf, int vf, bool kvarn,
+                               cudaStream_t st) {
+  if (kf != BF16 || vf != BF16 || kvarn) return cudaErrorNotSupported;
   if (head_dim == 64) return launch_decode_t<64, BF16, BF16, false>(a, st);
   if (head_dim == 128) return launch_decode_t<128, BF16, BF16, false>(a, st);
   return cudaErrorNotSupported;

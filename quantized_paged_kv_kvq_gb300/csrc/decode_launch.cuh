@@ -106,32 +106,41 @@ template <int D, int KF, int VF, bool KVARN>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   using C = DecodeCfg<D, KF, VF, KVARN>;
   if (tensor_map_encoder() == nullptr) return cudaErrorNotSupported;
-  DecodeMaps maps;
+  DecodeMaps<kMaxPageClasses> maps;
   memset(&maps, 0, sizeof(maps));
   const int hpc = a.heads_per_cta;
   DecodeArgs args = a;
-  // (8-token pages take per-head boxes: two land as one head's 16 rows)
-  args.one_box = a.block_size >= 16 &&
-                 encode_codes_map_headmajor(&maps.k, a.k_cache, C::KB, a.num_kv_heads,
-                                            a.block_size, a.num_blocks, hpc, C::K_SWZ) &&
-                 encode_codes_map_headmajor(&maps.v, a.v_cache, C::VB, a.num_kv_heads,
-                                            a.block_size, a.num_blocks, hpc, C::V_SWZ);
-  if (!args.one_box &&
-      (!encode_codes_map(&maps.k, a.k_cache, C::KB, a.num_kv_heads, a.block_size, a.num_blocks,
-                         C::K_SWZ) ||
-       !encode_codes_map(&maps.v, a.v_cache, C::VB, a.num_kv_heads, a.block_size, a.num_blocks,
-                         C::V_SWZ)))
-    return cudaErrorInvalidValue;
-  if (C::KMF > 0 && !encode_meta_map(&maps.km, a.k_meta, C::KMF, a.num_kv_heads, a.block_size,
-                                     a.num_blocks, hpc))
-    return cudaErrorInvalidValue;
-  if (C::VMF > 0 && !encode_meta_map(&maps.vm, a.v_meta, C::VMF, a.num_kv_heads, a.block_size,
-                                     a.num_blocks, hpc))
-    return cudaErrorInvalidValue;
+  // one head-major box per tile when every class's codes allow it (pages of 16
+  // tokens or more), else per-head boxes (8-token pages take two per head: they
+  // land as one head's 16 rows)
+  args.one_box = 1;
+  for (int c = 0; c < a.num_classes; ++c) {
+    const int bs = 1 << a.block_shift[c];
+    args.one_box = args.one_box && bs >= 16 &&
+                   encode_codes_map_headmajor(&maps.k[c], a.k_cache[c], C::KB, a.num_kv_heads, bs,
+                                              a.num_blocks[c], hpc, C::K_SWZ) &&
+                   encode_codes_map_headmajor(&maps.v[c], a.v_cache[c], C::VB, a.num_kv_heads, bs,
+                                              a.num_blocks[c], hpc, C::V_SWZ);
+  }
+  for (int c = 0; c < a.num_classes; ++c) {
+    const int bs = 1 << a.block_shift[c];
+    if (!args.one_box &&
+        (!encode_codes_map(&maps.k[c], a.k_cache[c], C::KB, a.num_kv_heads, bs, a.num_blocks[c],
+                           C::K_SWZ) ||
+         !encode_codes_map(&maps.v[c], a.v_cache[c], C::VB, a.num_kv_heads, bs, a.num_blocks[c],
+                           C::V_SWZ)))
+      return cudaErrorInvalidValue;
+    if (C::KMF > 0 && !encode_meta_map(&maps.km[c], a.k_meta[c], C::KMF, a.num_kv_heads, bs,
+                                       a.num_blocks[c], hpc))
+      return cudaErrorInvalidValue;
+    if (C::VMF > 0 && !encode_meta_map(&maps.vm[c], a.v_meta[c], C::VMF, a.num_kv_heads, bs,
+                                       a.num_blocks[c], hpc))
+      return cudaErrorInvalidValue;
+  }
 
-  auto kern_one = decode_partition_kernel<D, KF, VF, KVARN, false>;
-  auto kern_split = decode_partition_kernel<D, KF, VF, KVARN, true>;  // 8-token pages
-  auto kern = a.block_size < 16 ? kern_split : kern_one;
+  auto kern_one = decode_partition_kernel<D, KF, VF, KVARN, kPagesOne>;
+  auto kern_split = decode_partition_kernel<D, KF, VF, KVARN, kPages8>;
+  auto kern_mixed = decode_partition_kernel<D, KF, VF, KVARN, kPagesMixed>;
   const int smem = decode_smem_bytes<C>(hpc, a.gqa);
   static std::atomic<unsigned long long> attr_done{0};  // one bit per device
   int dev = 0;
@@ -139,15 +148,29 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_done.load() & bit)) {
-    for (auto k : {kern_one, kern_split}) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               decode_smem_bytes<C>(kHeadsPerCta, 8));
+    const int most = decode_smem_bytes<C>(kHeadsPerCta, 8);
+    for (const void* k : {reinterpret_cast<const void*>(kern_one),
+                          reinterpret_cast<const void*>(kern_split),
+                          reinterpret_cast<const void*>(kern_mixed)}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
       if (e != cudaSuccess) return e;
     }
     attr_done.fetch_or(bit);
   }
   const dim3 grid(a.num_ctas, a.num_kv_heads / hpc, 1);
-  kern<<<grid, hpc * 32, smem, st>>>(args, maps);
+  if (a.seq_class != nullptr) {  // a class array: the mixed instance (pages of 16 or more)
+    kern_mixed<<<grid, hpc * 32, smem, st>>>(args, maps);
+  } else {  // one pool: class 0's maps only
+    DecodeMaps<1> one;
+    one.k[0] = maps.k[0];
+    one.v[0] = maps.v[0];
+    one.km[0] = maps.km[0];
+    one.vm[0] = maps.vm[0];
+    if (a.block_shift[0] < 4)
+      kern_split<<<grid, hpc * 32, smem, st>>>(args, one);
+    else
+      kern_one<<<grid, hpc * 32, smem, st>>>(args, one);
+  }
   return cudaGetLastError();
 }
 

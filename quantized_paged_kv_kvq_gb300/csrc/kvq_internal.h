@@ -35,11 +35,21 @@ struct WriteArgs {
   float cR;  // float(1/sqrt(head_dim))
 };
 
+// Page classes of one decode call (pools of pages of one size each).
+constexpr int kMaxPageClasses = 2;
+
 struct DecodeArgs {
-  const uint8_t* k_cache;
-  const uint8_t* v_cache;
-  const __half* k_meta;
-  const __half* v_meta;
+  // The cache: one pool per page class (its codes, metadata, page size and
+  // block count); a cache of one page size has one.  seq_class[s] is the class
+  // of sequence s (nullptr: class 0), whose block ids index that pool.
+  const uint8_t* k_cache[kMaxPageClasses];
+  const uint8_t* v_cache[kMaxPageClasses];
+  const __half* k_meta[kMaxPageClasses];
+  const __half* v_meta[kMaxPageClasses];
+  int block_shift[kMaxPageClasses];  // log2(page size)
+  int num_blocks[kMaxPageClasses];
+  const uint8_t* seq_class;
+  int num_classes;
   const uint16_t* query;  // bf16 [S, Hq, D]
   uint16_t* out;          // bf16 [S, Hq, D]
   const int32_t* block_table;
@@ -58,9 +68,6 @@ struct DecodeArgs {
   int gqa;
   int heads_per_cta;  // kv-heads per CTA (= consumer warps), divides num_kv_heads
   int one_box;        // K / V tile loaded head-major by one TMA each (else per head)
-  int block_size;
-  int block_shift;  // log2(block_size)
-  int num_blocks;
   int max_blocks_per_seq;
   int max_context_len;
   int num_ctas;          // NC: stream-K ranges (CTAs per head group)
@@ -77,10 +84,10 @@ struct DecodeArgs {
   const uint16_t* new_value;
   int64_t new_key_stride;
   int64_t new_value_stride;
-  uint8_t* k_cache_w;  // the same caches, writable
-  uint8_t* v_cache_w;
-  __half* k_meta_w;
-  __half* v_meta_w;
+  uint8_t* k_cache_w[kMaxPageClasses];  // the same pools, writable
+  uint8_t* v_cache_w[kMaxPageClasses];
+  __half* k_meta_w[kMaxPageClasses];
+  __half* v_meta_w[kMaxPageClasses];
   float k_inv;  // 1/k_scale (symmetric formats, per-tensor scales)
   float v_inv;
   // Bounded pipeline waits: polls of an mbarrier before the CTA gives up (sets
@@ -98,22 +105,30 @@ cudaError_t launch_write_asym(const WriteArgs& a, int head_dim, int kf, int vf, 
                               cudaStream_t st);
 bool write_supported(int kf, int vf, bool kvarn);
 
-cudaError_t launch_decode_d64_sym(const DecodeArgs& a, int kf, int vf, cudaStream_t st);
-cudaError_t launch_decode_d128_sym(const DecodeArgs& a, int kf, int vf, cudaStream_t st);
-cudaError_t launch_decode_d64_asym(const DecodeArgs& a, int kf, int vf, bool kvarn,
-                                   cudaStream_t st);
-cudaError_t launch_decode_d128_asym(const DecodeArgs& a, int kf, int vf, bool kvarn,
-                                    cudaStream_t st);
-cudaError_t launch_decode_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st);
+// Decode launchers, one per translation unit of kernel instances: each returns
+// cudaErrorNotSupported for a (head_dim, formats, KVarN) it does not hold.
+using DecodeLauncher = cudaError_t (*)(const DecodeArgs& a, int head_dim, int kf, int vf,
+                                       bool kvarn, cudaStream_t st);
+#define KVQ_DECODE_UNITS(X) \
+  X(decode_d64_sym)         \
+  X(decode_d64_fp8k)        \
+  X(decode_d64_asym)        \
+  X(decode_d64_kvarn)       \
+  X(decode_d128_sym)        \
+  X(decode_d128_fp8k)       \
+  X(decode_d128_asym)       \
+  X(decode_d128_kvarn)      \
+  X(decode_bf16)
+#define KVQ_DECLARE_UNIT(U)                                                                  \
+  cudaError_t launch_##U(const DecodeArgs& a, int head_dim, int kf, int vf, bool kvarn,      \
+                         cudaStream_t st);                                                   \
+  cudaError_t take_error_bits_##U(unsigned* bits);
+KVQ_DECODE_UNITS(KVQ_DECLARE_UNIT)
+#undef KVQ_DECLARE_UNIT
 
-// read-and-clear of each translation unit's device error word
+// read-and-clear of the write units' device error words
 cudaError_t take_error_bits_write(unsigned* bits);
 cudaError_t take_error_bits_write_asym(unsigned* bits);
-cudaError_t take_error_bits_decode_d64_sym(unsigned* bits);
-cudaError_t take_error_bits_decode_d128_sym(unsigned* bits);
-cudaError_t take_error_bits_decode_d64_asym(unsigned* bits);
-cudaError_t take_error_bits_decode_d128_asym(unsigned* bits);
-cudaError_t take_error_bits_decode_bf16(unsigned* bits);
 
 cudaError_t launch_hadamard(void* x, int dtype, int64_t rows, int head_dim, const int8_t* signs,
                             int inverse, float cR, cudaStream_t st);

@@ -27,6 +27,7 @@ DEVERR_BLOCK_RANGE = 2
 DEVERR_CONTEXT_RANGE = 4
 DEVERR_COMBINE = 8
 DEVERR_TIMEOUT = 16
+DEVERR_CLASS_RANGE = 32
 
 
 class KvqError(RuntimeError):
@@ -62,6 +63,9 @@ SIGNATURES = {
                                  _P, _I32, _F32, _I32, _P, _SZ, _P]),
     "kvq_paged_decode_static": (_I32, [_DESC, _P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _I32,
                                        _F32, _I32, _P]),
+    "kvq_decode_mixed": (_I32, [_DESC, _I32, ctypes.POINTER(_P), ctypes.POINTER(_P), _P, _P, _P,
+                                _I64, _I64, _P, _P, _I32, _I32, _P, _I32, _P, _I32, _F32, _I32,
+                                _P, _SZ, _P]),
     "kvq_paged_decode_static_capacity": (_SZ, []),
     "kvq_hadamard": (_I32, [_P, _I32, _I64, _I32, _P, _I32, _P]),
     "kvq_calibrate_scale": (_I32, [_P, _I64, _F32, _P, _P]),
@@ -255,6 +259,38 @@ def kvq_decode_append(cache: KVCache, new_key: torch.Tensor, new_value: torch.Te
                                max_context_len, float(sm_scale), num_ctas, _ptr(workspace),
                                ws_bytes, _stream(stream))
     _check(st, "kvq_decode_append")
+    return out
+
+
+def kvq_decode_mixed(classes, seq_class: torch.Tensor, query: torch.Tensor, out: torch.Tensor,
+                     block_table: torch.Tensor, context_lens: torch.Tensor, max_context_len: int,
+                     sm_scale: float, workspace: Optional[torch.Tensor] = None,
+                     num_ctas: int = 0, new_key: Optional[torch.Tensor] = None,
+                     new_value: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode (or, with new_key / new_value, the fused append step) over a cache
+    of several page classes: `classes` is a list of KVCache, one pool per page
+    size; seq_class (uint8 [S]) names each sequence's class, and block_table
+    row s holds block ids of that class's pool."""
+    lib = load_library()
+    assert seq_class.dtype == torch.uint8 and seq_class.is_contiguous()
+    assert query.dtype == torch.bfloat16 and out.dtype == torch.bfloat16
+    assert query.is_contiguous() and out.is_contiguous()
+    assert block_table.dtype == torch.int32 and context_lens.dtype == torch.int32
+    assert block_table.is_contiguous()
+    n = len(classes)
+    descs = (_CacheDesc * n)(*[c.desc() for c in classes])
+    kcs = (ctypes.c_void_p * n)(*[c.k_cache.data_ptr() for c in classes])
+    vcs = (ctypes.c_void_p * n)(*[c.v_cache.data_ptr() for c in classes])
+    s, hq, _ = query.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ks = 0 if new_key is None else new_key.stride(0)
+    vs = 0 if new_value is None else new_value.stride(0)
+    st = lib.kvq_decode_mixed(descs, n, kcs, vcs, _ptr(seq_class), _ptr(new_key),
+                              _ptr(new_value), ks, vs, _ptr(out), _ptr(query), s, hq,
+                              _ptr(block_table), block_table.shape[1], _ptr(context_lens),
+                              max_context_len, float(sm_scale), num_ctas, _ptr(workspace),
+                              ws_bytes, _stream(stream))
+    _check(st, "kvq_decode_mixed")
     return out
 
 

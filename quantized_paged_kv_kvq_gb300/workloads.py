@@ -281,6 +281,49 @@ def device_data(wl: Workload, device, seed: Optional[int] = None) -> dict:
                 query=query.to(torch.bfloat16))
 
 
+def mixed_pages(wl: Workload, block_sizes=(16, 64), seed: Optional[int] = None,
+                spare_blocks: int = 4) -> dict:
+    """Lay wl's sequences out over page classes of different sizes (one pool per
+    class): sequence s takes a seeded class; its pages are a random permutation
+    within that class's pool.  Returns seq_class (uint8 [S]), block_table
+    (int32 [S, max_context_len / smallest page size], ids in the sequence's
+    pool, -1 past its pages),
+    num_blocks per class, and per class the token indices (into wl's token
+    order, sequences concatenated) and their slots in that pool."""
+    rng = np.random.Generator(np.random.PCG64([wl.seed if seed is None else seed, 4]))
+    S = wl.num_seqs
+    seq_class = rng.integers(0, len(block_sizes), size=S).astype(np.uint8)
+    need = [(int(c) + block_sizes[k] - 1) // block_sizes[k]
+            for c, k in zip(wl.context_lens, seq_class)]
+    # the table is as wide as max_context_len at the smallest page size
+    width = max(-(-int(wl.max_context_len) // min(block_sizes)), 1)
+    table = np.full((S, width), -1, np.int32)
+    num_blocks = []
+    for k, bs in enumerate(block_sizes):
+        members = [s for s in range(S) if seq_class[s] == k]
+        total = sum(need[s] for s in members) + spare_blocks
+        perm = rng.permutation(total).astype(np.int32)
+        pos = 0
+        for s in members:
+            table[s, :need[s]] = perm[pos:pos + need[s]]
+            pos += need[s]
+        num_blocks.append(total)
+    starts = np.concatenate([[0], np.cumsum(wl.context_lens.astype(np.int64))])
+    tokens, slots = [], []
+    for k, bs in enumerate(block_sizes):
+        idx, sl = [], []
+        for s in range(S):
+            if seq_class[s] != k:
+                continue
+            t = np.arange(int(wl.context_lens[s]), dtype=np.int64)
+            idx.append(starts[s] + t)
+            sl.append(table[s, t // bs].astype(np.int64) * bs + t % bs)
+        tokens.append(np.concatenate(idx) if idx else np.zeros(0, np.int64))
+        slots.append(np.concatenate(sl) if sl else np.zeros(0, np.int64))
+    return dict(seq_class=seq_class, block_table=table, num_blocks=num_blocks,
+                block_sizes=tuple(block_sizes), tokens=tokens, slots=slots)
+
+
 def prefill_chunk(wl: Workload, num_tokens: int, seed: int) -> dict:
     """A prefill chunk of `num_tokens` new tokens for sequence 0 of `wl`,
     written at positions [0, num_tokens) of that sequence's blocks."""

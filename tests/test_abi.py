@@ -183,3 +183,23 @@ def test_bf16_cache_validation(lib):
     assert _write(lib, _desc(k_fmt=6, v_fmt=6, flags=1)) == 2
     assert _write(lib, _desc(k_fmt=6, v_fmt=6, k_head_scales=FAKE)) == 1
     assert _write(lib, _desc(k_fmt=7, v_fmt=7)) == 1
+
+
+def test_mixed_pages_validation(lib):
+    """The classes of a mixed cache share formats and heads; pages of 16 tokens
+    or more; one or two classes."""
+    K = ctypes.c_void_p * 2
+    kcs, vcs = K(FAKE, FAKE), K(FAKE, FAKE)
+
+    def call(descs, n=2, cls=FAKE):
+        arr = (type(descs[0]) * len(descs))(*descs)
+        return lib.kvq_decode_mixed(arr, n, kcs, vcs, cls, None, None, 0, 0, FAKE, FAKE, 4, 32,
+                                    FAKE, 64, FAKE, 1024, 0.088, 256, None, 0, None)
+    assert call([_desc(), _desc(block_size=64)]) == 3  # valid: needs a workspace
+    assert call([_desc(), _desc(block_size=64)], cls=None) == 1
+    assert call([_desc(), _desc(block_size=8)]) == 2  # 8-token pages: one class per call
+    assert call([_desc(), _desc(k_fmt=2)]) == 1  # formats differ
+    assert call([_desc(), _desc(num_kv_heads=4)]) == 1
+    assert call([_desc(), _desc(k_scale=0.2)]) == 1
+    assert call([_desc(), _desc()], n=3) == 2
+    assert call([_desc(), _desc()], n=0) == 2

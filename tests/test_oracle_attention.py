@@ -158,3 +158,45 @@ def test_empty_context_gives_zero():
     kc, km, vc, vm, ks, vs = _write_all(wl)
     out = _decode(wl, kc, km, vc, vm, ks, vs)
     assert np.all(out[0] == 0) and np.all(out[2] == 0) and np.any(out[1] != 0)
+
+
+def test_mixed_page_classes_give_the_single_class_result():
+    from oracle import attention as OA
+    """Attention does not depend on page sizes: the same tokens written into two
+    pools of 16- and 64-token pages (each sequence in one pool) decode to
+    exactly the result of one pool of 16-token pages, and the layout puts every
+    token at its own slot of its own class."""
+    from oracle import cache as OC
+    from oracle import formats as OF
+    from quantized_paged_kv_kvq_gb300 import workloads as W
+    for name in ("llama8b_int8", "llama70b_int4", "kvarn_131k"):
+        wl = W.workload(name, num_seqs=5, ctx_lo=1, ctx_hi=150, num_q_heads=8, num_kv_heads=2)
+        mp = W.mixed_pages(wl, (16, 64))
+        assert set(np.unique(mp["seq_class"])) <= {0, 1}
+        for c, bs in enumerate(mp["block_sizes"]):  # slots are distinct and inside the pool
+            assert np.unique(mp["slots"][c]).size == mp["slots"][c].size
+            assert mp["slots"][c].size == 0 or mp["slots"][c].max() < mp["num_blocks"][c] * bs
+        ks = OF.calibrate(wl.key, wl.k_scale_rule) if wl.k_scale_rule else np.float32(1)
+        vs = OF.calibrate(wl.value, wl.v_scale_rule) if wl.v_scale_rule else np.float32(1)
+        classes = []
+        for c, bs in enumerate(mp["block_sizes"]):
+            kc, km = OC.alloc_cache(mp["num_blocks"][c], bs, 2, wl.head_dim, wl.k_fmt, wl.kvarn)
+            vc, vm = OC.alloc_cache(mp["num_blocks"][c], bs, 2, wl.head_dim, wl.v_fmt, wl.kvarn)
+            t = mp["tokens"][c]
+            OC.write_cache(kc, km, wl.key[t], mp["slots"][c], bs, wl.k_fmt, ks, wl.kvarn, wl.signs)
+            OC.write_cache(vc, vm, wl.value[t], mp["slots"][c], bs, wl.v_fmt, vs, wl.kvarn,
+                           wl.signs)
+            classes.append((kc, km, vc, vm, bs))
+        sm = OA.default_sm_scale(wl.head_dim)
+        got = OA.paged_decode_classes(wl.query, classes, mp["seq_class"], mp["block_table"],
+                                      wl.context_lens, wl.k_fmt, wl.v_fmt, ks, vs, sm, wl.kvarn,
+                                      wl.signs)
+        kc, km = OC.alloc_cache(wl.num_blocks, wl.block_size, 2, wl.head_dim, wl.k_fmt, wl.kvarn)
+        vc, vm = OC.alloc_cache(wl.num_blocks, wl.block_size, 2, wl.head_dim, wl.v_fmt, wl.kvarn)
+        OC.write_cache(kc, km, wl.key, wl.slot_mapping, wl.block_size, wl.k_fmt, ks, wl.kvarn,
+                       wl.signs)
+        OC.write_cache(vc, vm, wl.value, wl.slot_mapping, wl.block_size, wl.v_fmt, vs, wl.kvarn,
+                       wl.signs)
+        ref = OA.paged_decode(wl.query, kc, km, vc, vm, wl.block_table, wl.context_lens,
+                              wl.block_size, wl.k_fmt, wl.v_fmt, ks, vs, sm, wl.kvarn, wl.signs)
+        assert np.array_equal(got, ref), name
