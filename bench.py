@@ -73,6 +73,11 @@ def kv_bytes_per_token(wl) -> int:
     return wl.num_kv_heads * per_head
 
 
+def kv_cache_bytes(case) -> int:
+    """Bytes of the cached codes and metadata a decode reads."""
+    return int(case.wl.context_lens.astype("int64").sum()) * kv_bytes_per_token(case.wl)
+
+
 def decode_bytes(wl) -> int:
     """Codes + metadata of every context token (once, whatever the GQA ratio),
     the query, the output, the used block-table entries and the lengths."""
@@ -403,7 +408,7 @@ class Case:
         import torch
         from quantized_paged_kv_kvq_gb300 import kvq
         from quantized_paged_kv_kvq_gb300 import workloads as W
-        self.kvq, self.dev, self.ctas = kvq, dev, ctas
+        self.kvq, self.dev, self.ctas, self.l2_bytes = kvq, dev, ctas, l2_bytes
         self.wl = wl = W.workload(name, seed=seed, with_data=False)
         data = W.device_data(wl, dev, seed)
         self.key, self.value, self.query = data["key"], data["value"], data["query"]
@@ -512,6 +517,23 @@ def time_write_back_to_back(case, launches):
     e0.record()
     for _ in range(launches):
         case.write()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / launches
+
+
+def time_decode_back_to_back(case, launches):
+    """Decodes one after another with no flush between them, between one pair
+    of events (the launch overhead of all but the first is hidden behind the
+    previous kernel, as in a serving loop).  Where the cache is larger than L2,
+    each launch still reads it from DRAM (the loads carry an evict-first
+    policy); a smaller cache stays in L2 and the number is not an HBM one."""
+    import torch
+    case.flush_l2()
+    e0, e1 = _events(2)
+    e0.record()
+    for _ in range(launches):
+        case.decode()
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) * 1e3 / launches
@@ -689,6 +711,7 @@ def measure_case(args, case, rank, world, hbm, peak_note, steps, headline=False)
     dbytes, wbytes = decode_bytes(wl), write_bytes(wl)
     pct = lambda x: {f"p{q}": round(float(np.percentile(x, q)) * 1e3, 3) for q in (10, 50, 90)}
     b2b = max_over_ranks([time_write_back_to_back(case, max(8, min(steps, 50)))], dev)[0]
+    d2b = max_over_ranks([time_decode_back_to_back(case, max(8, min(steps, 200)))], dev)[0]
     n_side = max(3, min(steps, 200))
     app = None if args.no_append else time_append(case, n_side)
     chunk = time_chunk(case, args.chunk_tokens, n_side, W_SEED(wl.name) + 7 + 100 * rank, hbm)
@@ -706,6 +729,9 @@ def measure_case(args, case, rank, world, hbm, peak_note, steps, headline=False)
         "write_bytes": wbytes,
         "cache_write_back_to_back_us": b2b,
         "cache_write_back_to_back_frac_of_hbm": wbytes / (b2b * 1e-6) / 1e9 / hbm,
+        "decode_back_to_back_us": d2b,
+        "decode_back_to_back_frac_of_hbm": dbytes / (d2b * 1e-6) / 1e9 / hbm,
+        "decode_back_to_back_cache_exceeds_l2": kv_cache_bytes(case) > case.l2_bytes,
         "roofline_decode": roofline("decode_partition", wl.name, dbytes, t_dec / steps, hbm,
                                     peak_note),
         "roofline_write": roofline(write_kernel_name(wl), wl.name, wbytes, t_write / steps, hbm,
@@ -822,6 +848,8 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
         "cache_write_frac_of_hbm": head["cache_write_frac_of_hbm"],
         "cache_write_back_to_back_us": head["cache_write_back_to_back_us"],
         "cache_write_back_to_back_frac_of_hbm": head["cache_write_back_to_back_frac_of_hbm"],
+        "decode_back_to_back_us": head["decode_back_to_back_us"],
+        "decode_back_to_back_frac_of_hbm": head["decode_back_to_back_frac_of_hbm"],
         "decode_bytes": head["decode_bytes"], "write_bytes": head["write_bytes"],
         "wall_s_timed_region": head["wall_s_timed_region"],
         # the dominant kernel of the step (largest share of its time) first

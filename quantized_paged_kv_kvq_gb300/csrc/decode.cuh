@@ -78,7 +78,9 @@ struct DecodeCfg {
     return align(hpc * K_HEAD) + align(hpc * V_HEAD) + align(meta_room(hpc, KMF) + meta_room(hpc, VMF));
   }
   static constexpr int STAGE_MAX = stage_bytes(kHeadsPerCta);
-  static constexpr int STAGES = STAGE_MAX >= 24576 ? 3 : STAGE_MAX >= 16384 ? 5 : 6;
+  // ring depth: about 96 KB of tiles per CTA with two CTAs per SM; KVarN runs
+  // one CTA per SM (its registers) with six stages
+  static constexpr int STAGES = KVARN ? 6 : STAGE_MAX >= 24576 ? 3 : STAGE_MAX >= 16384 ? 5 : 6;
   static constexpr int EB = KF == BF16 ? 2 : 1;  // K element bytes (INT4: see kslot_d)
   static constexpr bool KVARN_ = KVARN;
   static_assert(KW * 4 == K_LANE && VW * 4 == VPS, "layout");
@@ -745,8 +747,11 @@ __device__ __forceinline__ void append_new_tokens(const DecodeArgs& a, long long
 // pages: a tile is two pages) or kPagesMixed (each sequence in the pool of its
 // page class); separate instances, so that one page size keeps the one-box
 // path's registers.
+// Two CTAs per SM (128 registers a thread), except the 16-bit cache (its
+// stages fill shared memory) and KVarN (the rotation and its metadata need
+// more registers): one.
 template <int D, int KF, int VF, bool KVARN, int PAGES>
-__global__ void __launch_bounds__(kHeadsPerCta * 32, KF == BF16 ? 1 : 2)
+__global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 : 2)
     decode_partition_kernel(const DecodeArgs a, const __grid_constant__ DecodeMapsOf<PAGES> maps) {
   using C = DecodeCfg<D, KF, VF, KVARN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
