@@ -27,8 +27,8 @@
  *    storage in write_to_paged_cache, paged attention taking k_scale,
  *    k_zeropoint, v_scale, v_zeropoint;
  *  - "KVarN : le backend natif pour la quantification du cache KV" (section
- *    'Contexte Technique'): Hadamard rotation + variance normalisation +
- *    asymmetric quantization, no calibration.
+ *    'Contexte Technique'): a Hadamard rotation and a variance normalisation
+ *    before asymmetric codes, with no calibration step.
  */
 #ifndef KVQ_H
 #define KVQ_H

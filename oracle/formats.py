@@ -9,9 +9,9 @@ Formats and the passages they follow:
 * INT8, symmetric, one fp32 scale per tensor (per layer):
   "vllm-int8-kv-cache-for-ampere-sm86" project summary -- an INT8 KV cache
   with calibrated per-layer scaling values.
-* FP8 E4M3 (the "FP8-E4M3 emulation for one part of the cache" of the same
-  summary; `fp8` = `fp8_e4m3` in vLLM PR #4893 'Load FP8 kv-cache scaling
-  factors from checkpoints', item 1) and FP8 E5M2 (same item), each with a
+* FP8 E4M3 (the same summary emulates E4M3 for a part of the cache;
+  `fp8` = `fp8_e4m3` in vLLM PR #4893 'Load FP8 kv-cache scaling factors
+  from checkpoints', item 1) and FP8 E5M2 (same item), each with a
   kv_scale; uncalibrated means scale 1.0 (PR #4893 item 2; the modelium guide
   'vLLM FP8 KV-кеш', section 'Что проверить перед сменой dtype?').
   Bit layouts follow the OCP 8-bit floating point definition: E4M3FN (bias 7,
