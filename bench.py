@@ -539,6 +539,51 @@ def time_decode_back_to_back(case, launches):
     return e0.elapsed_time(e1) * 1e3 / launches
 
 
+def time_decode_graph(case, n, reps=3):
+    """Decode time per launch when the steps are replayed from a CUDA graph, as
+    a serving loop launches its decode: one graph of n x (L2 flush, decode) and
+    one of the n flushes alone, each replayed between a pair of events; the
+    difference over n.  The flush before every launch stays, so each decode
+    still reads the cache from DRAM."""
+    import torch
+    s = torch.cuda.Stream(device=case.dev)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            fn()  # warm-up outside the capture (first-use allocations)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        return g
+
+    def both():
+        for _ in range(n):
+            case.flush_l2()
+            case.decode()
+
+    def flushes():
+        for _ in range(n):
+            case.flush_l2()
+
+    def replay_us(g):
+        ts = []
+        for _ in range(reps):
+            e0, e1 = _events(2)
+            torch.cuda.synchronize()
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return sorted(ts)[len(ts) // 2]
+
+    ga, gb = capture(both), capture(flushes)
+    us = (replay_us(ga) - replay_us(gb)) / n
+    del ga, gb
+    return us
+
+
 def time_each(case, fn, n, warmup=3):
     """Median (us) of `fn` over n launches, L2 flushed before each."""
     import numpy as np
@@ -712,6 +757,7 @@ def measure_case(args, case, rank, world, hbm, peak_note, steps, headline=False)
     pct = lambda x: {f"p{q}": round(float(np.percentile(x, q)) * 1e3, 3) for q in (10, 50, 90)}
     b2b = max_over_ranks([time_write_back_to_back(case, max(8, min(steps, 50)))], dev)[0]
     d2b = max_over_ranks([time_decode_back_to_back(case, max(8, min(steps, 200)))], dev)[0]
+    dgr = max_over_ranks([time_decode_graph(case, max(4, min(steps, 50)))], dev)[0]
     n_side = max(3, min(steps, 200))
     app = None if args.no_append else time_append(case, n_side)
     chunk = time_chunk(case, args.chunk_tokens, n_side, W_SEED(wl.name) + 7 + 100 * rank, hbm)
@@ -732,6 +778,8 @@ def measure_case(args, case, rank, world, hbm, peak_note, steps, headline=False)
         "decode_back_to_back_us": d2b,
         "decode_back_to_back_frac_of_hbm": dbytes / (d2b * 1e-6) / 1e9 / hbm,
         "decode_back_to_back_cache_exceeds_l2": kv_cache_bytes(case) > case.l2_bytes,
+        "decode_graph_us": dgr,
+        "decode_graph_frac_of_hbm": dbytes / (dgr * 1e-6) / 1e9 / hbm,
         "roofline_decode": roofline("decode_partition", wl.name, dbytes, t_dec / steps, hbm,
                                     peak_note),
         "roofline_write": roofline(write_kernel_name(wl), wl.name, wbytes, t_write / steps, hbm,
@@ -850,6 +898,8 @@ def run_kvq(args, rank: int, world: int, local_rank: int):
         "cache_write_back_to_back_frac_of_hbm": head["cache_write_back_to_back_frac_of_hbm"],
         "decode_back_to_back_us": head["decode_back_to_back_us"],
         "decode_back_to_back_frac_of_hbm": head["decode_back_to_back_frac_of_hbm"],
+        "decode_graph_us": head["decode_graph_us"],
+        "decode_graph_frac_of_hbm": head["decode_graph_frac_of_hbm"],
         "decode_bytes": head["decode_bytes"], "write_bytes": head["write_bytes"],
         "wall_s_timed_region": head["wall_s_timed_region"],
         # the dominant kernel of the step (largest share of its time) first
