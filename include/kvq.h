@@ -172,6 +172,11 @@ kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_se
  *   (may be NULL when that size is 0), 16-byte aligned; its contents on entry
  *   do not matter (its completion tags and claims carry a per-call value).  Two
  *   calls that overlap on the GPU must not share a workspace.
+ * CUDA graphs: a call made while its stream is capturing first records a
+ *   memset of the workspace's tags and claims (a few KB), so every replay of
+ *   the graph starts from clear words (a replay reuses the recorded call's
+ *   value).  This holds for kvq_paged_decode(_ex), kvq_decode_append,
+ *   kvq_decode_mixed and kvq_paged_decode_static.
  * One kernel launch, stream-K: each CTA owns an equal contiguous range of the
  *   16-token tiles of all sequences (for a group of up to 8 kv-heads).  A
  *   sequence split between CTAs leaves partial results that are merged

@@ -360,6 +360,22 @@ kvq_status decode_call(const kvq_cache_desc* classes, int32_t num_classes,
     a.withhold_cta = g_wait_hook_cta.load();
     a.withhold_tile = g_wait_hook_tile.load();
   }
+  // A launch recorded into a CUDA graph is replayed with the same call tag, so
+  // a replay would find the tags and claims its predecessor left: while the
+  // stream is capturing, the call first clears them (a memset node that runs
+  // before the kernel at every replay).  Direct calls take a fresh tag instead.
+  if (need > 0) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    if (cap == cudaStreamCaptureStatusActive) {
+      const size_t words = 3 * slot_words + static_cast<size_t>(num_seqs) *
+                                                (cache->num_kv_heads / heads_per_cta(cache->num_kv_heads));
+      if (cudaMemsetAsync(a.tags, 0, words * sizeof(unsigned long long),
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    }
+  }
   cudaError_t e = cudaErrorNotSupported;
   const int kf = cache->k_fmt, vf = cache->v_fmt;
 #define KVQ_UNIT_LAUNCHER(U) launch_##U,
