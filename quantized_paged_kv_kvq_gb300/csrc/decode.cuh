@@ -419,6 +419,7 @@ struct Cursor {
   int nx, nx_ctx;  // next sequence of the range with tokens (num_seqs: none)
   int i;           // loads issued
   int cls;         // page class of sequence s
+  int lam;         // weighted start of sequence s (the partition's line)
 };
 
 static_assert(sizeof(Cursor) <= 48, "the cursor lives in scratch words 16..21");
@@ -450,7 +451,7 @@ struct TileHeader {
   int ps;      // global index of the sequence's first tile
   int tiles;   // tiles of the sequence
   int next_s;  // sequence of the range's next segment (first tiles only), or -1
-  int pad;
+  int lam;     // weighted start of the sequence on the partition's line
 };
 
 __device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
@@ -479,13 +480,46 @@ __device__ __forceinline__ long long div_floor(long long n, long long d) {
     return static_cast<unsigned>(n) / static_cast<unsigned>(d);
   return n / d;
 }
-// First global tile of stream-K range k: ranges [k*T/NC, (k+1)*T/NC).
-__device__ __forceinline__ long long range_start(const DecodeArgs& a, long long T, int k) {
-  return div_floor(T * k, a.num_ctas);
+// ---- Stream-K partition.  The tiles lie on a weighted line: each sequence with
+// tokens takes kBoundaryWeight (the cost of starting and ending a segment),
+// then kTileWeight per tile, so a range that holds a sequence boundary gets
+// fewer tiles.  The line (total weight W) is cut at cut(k) = floor(W k / NC);
+// a tile belongs to the range whose interval holds its weighted start.  The
+// partition is a fixed function of the lengths and NC.
+constexpr int kTileWeight = 4;
+constexpr int kBoundaryWeight = 6;  // 1.5 tiles: what a boundary costs a range (measured)
+
+__device__ __forceinline__ long long cut(const DecodeArgs& a, long long W, int k) {
+  return div_floor(W * k, a.num_ctas);
 }
-// The range holding global tile x < T: the largest k with range_start(k) <= x.
-__device__ __forceinline__ int range_of(const DecodeArgs& a, long long x, long long T) {
-  return static_cast<int>(div_floor((x + 1) * a.num_ctas - 1, T));
+// The range holding weighted position w < W: the largest k with cut(k) <= w.
+__device__ __forceinline__ int range_of_w(const DecodeArgs& a, long long w, long long W) {
+  return static_cast<int>(div_floor((w + 1) * a.num_ctas - 1, W));
+}
+// A sequence on the weighted line: weighted start lam, first global tile ps,
+// v tiles, boundary weight c; its tile t starts at lam + c + kTileWeight * t.
+struct SeqSpan {
+  long long lam, ps;
+  int v, c;
+};
+// Tiles of the sequence whose weighted start lies before w.
+__device__ __forceinline__ long long tiles_before(const SeqSpan& q, long long w) {
+  const long long d = w - q.lam - q.c;
+  if (d <= 0) return 0;
+  const long long t = (d + kTileWeight - 1) / kTileWeight;
+  return t < q.v ? t : q.v;
+}
+// Whether ranges [k0, k1) hold a tile of the sequence.
+__device__ __forceinline__ bool holds_tiles(const DecodeArgs& a, long long W, const SeqSpan& q,
+                                            int k0, int k1) {
+  return tiles_before(q, cut(a, W, k0)) < tiles_before(q, cut(a, W, k1));
+}
+// The ranges of the sequence's first and last tiles.
+__device__ __forceinline__ int first_range(const DecodeArgs& a, long long W, const SeqSpan& q) {
+  return range_of_w(a, q.lam + q.c, W);
+}
+__device__ __forceinline__ int last_range(const DecodeArgs& a, long long W, const SeqSpan& q) {
+  return range_of_w(a, q.lam + q.c + static_cast<long long>(kTileWeight) * (q.v - 1), W);
 }
 
 template <int N>
@@ -525,16 +559,17 @@ __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
 constexpr int kTeam = 8;       // ranges merged together at the first level of a tree
 constexpr int kTreeRanges = 32;  // sequences over more ranges than this merge in two levels
 
-// Slot of range kk for the sequence whose tiles start at global tile ps: the
-// range's first segment (0) or its last (1).
-__device__ __forceinline__ long long slot_index(const DecodeArgs& a, long long T, long long ps,
+// Slot of range kk for the sequence q: the range's first segment (0) when the
+// range starts inside the sequence (the previous sequence's last tile, at
+// weighted start q.lam - kTileWeight, lies before the cut), else its last (1).
+__device__ __forceinline__ long long slot_index(const DecodeArgs& a, long long W, const SeqSpan& q,
                                                 int kk, int HG, int hg) {
-  return (static_cast<long long>(kk) * HG + hg) * 2 + (range_start(a, T, kk) >= ps ? 0 : 1);
+  return (static_cast<long long>(kk) * HG + hg) * 2 + (cut(a, W, kk) > q.lam - kTileWeight ? 0 : 1);
 }
 
 // Log-sum-exp merge of slots, by the whole CTA (warp w merges its kv-head's G
 // query heads, four at a time).  The inputs are the slots of ranges r_first +
-// step*i (i < count) for the sequence starting at global tile ps, skipping a
+// step*i (i < count) for the sequence q, skipping a
 // range whose span of `step` ranges (clipped at r_last) holds no tile.  A slot
 // holds, per query head, the normalised output acc/l in fp16 and (m, l) in
 // fp32; the merge is out = sum_i 2^(m_i - M) l_i (acc_i/l_i) / sum_i 2^(m_i - M) l_i.
@@ -544,8 +579,8 @@ __device__ __forceinline__ long long slot_index(const DecodeArgs& a, long long T
 // load of a warp reads whole 128-byte lines; each lane reads every slot's
 // (m, l) itself, and the loads of PU slots are issued together.
 template <int D, bool KVARN>
-__device__ __forceinline__ void merge_slots(const DecodeArgs& a, int s, long long ps, long long T,
-                                            int HG, int hg, int warp, int lane, int hpc,
+__device__ __forceinline__ void merge_slots(const DecodeArgs& a, int s, const SeqSpan& q,
+                                            long long W, int HG, int hg, int warp, int lane, int hpc,
                                             int r_first, int step, int count, int r_last,
                                             long long dst) {
   constexpr int LQ = 8;        // lanes per query head
@@ -568,9 +603,8 @@ __device__ __forceinline__ void merge_slots(const DecodeArgs& a, int s, long lon
       long long base = -1;
       if (c0 + lane < count) {
         const int kk = r_first + step * (c0 + lane);
-        const long long r0 = range_start(a, T, kk);
-        const long long r1 = range_start(a, T, min(kk + step, r_last + 1));
-        if (r0 < r1) base = slot_index(a, T, ps, kk, HG, hg) * rows;
+        if (holds_tiles(a, W, q, kk, min(kk + step, r_last + 1)))
+          base = slot_index(a, W, q, kk, HG, hg) * rows;
       }
       const int cn = min(32, count - c0);
 #pragma unroll 1
@@ -783,11 +817,14 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
   const uint32_t empty_s = full_s + 8 * C::STAGES;
   long long* scratch =
       reinterpret_cast<long long*>(smem + hdr_off + C::STAGES * (sizeof(TileHeader) + 16));
-  // scratch: [0] T, [1] first sequence, [2] its first tile, [3] R1, [4..12) scan,
+  // scratch: [0] W (the partition line's length), [1] first sequence, [2] its
+  // first tile, [3] R1, [4..12) scan,
   // [12..16) partial segments: (first tile, sequence << 32 | tiles) per end of the range,
   // [16..22) producer cursor, [22] second page id, [23] abort flag (int),
   // [24] withheld tile (int; test hook), [25] per end of the range: warps whose
-  // rows of the partial slot are stored (two ints)
+  // rows of the partial slot are stored (two ints), [26..28) range bounds and the
+  // first sequence's weighted start (prologue), [28..30) per end of the range:
+  // the weighted start of its sequence, [30] the boundary weight
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(scratch + 23);
   int* const done_warps = reinterpret_cast<int*>(scratch + 25);
   const int spin = a.spin_limit;
@@ -814,12 +851,19 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     }
   }
 
-  // ---- total tiles T and the range's first sequence (block scan of tile counts)
-  long long T = 0;
+  // ---- the range [R0, R1) of global tiles and its first sequence: a block scan
+  // of (sequences with tokens, tiles) gives each sequence its first tile and
+  // weighted start; the sequence whose weighted span holds cut(k) gives R0
+  // (and cut(k+1) R1); then the sequence holding tile R0.  With more sequences
+  // than threads the chunked scan below charges no boundary weight.
+  long long T = 0, Wt = 0;
+  int bw = kBoundaryWeight;
+  long long R0 = 0, R1 = 0;
   if (S <= static_cast<int>(blockDim.x)) {  // one pass: a sequence per thread
     const int s = threadIdx.x;
     const long long v = s < S ? seq_tiles(a, s) : 0;
-    long long incl = v;
+    const long long pk = v > 0 ? (1ll << 40) | v : 0;  // (sequences with tokens, tiles)
+    long long incl = pk;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const long long y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -827,19 +871,39 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     }
     if (lane == 31) scratch[4 + warp] = incl;
     __syncthreads();
-    long long before = 0;
+    long long before = 0, tot = 0;
     for (int w = 0; w < hpc; ++w) {
       const long long x = scratch[4 + w];
-      T += x;
+      tot += x;
       if (w < warp) before += x;
     }
-    const long long r0 = range_start(a, T, k), excl = before + incl - v;
-    if (v > 0 && excl <= r0 && r0 < excl + v) {
+    const long long mask = (1ll << 40) - 1;
+    T = tot & mask;
+    Wt = static_cast<long long>(kTileWeight) * T + bw * (tot >> 40);
+    const long long ex = before + incl - pk;  // exclusive prefix
+    const SeqSpan q{static_cast<long long>(kTileWeight) * (ex & mask) + bw * (ex >> 40), ex & mask,
+                    static_cast<int>(v), bw};
+    const long long lam_end = q.lam + kTileWeight * v + bw;
+    __syncthreads();  // every thread has read the scan words
+    const long long c0 = cut(a, Wt, k), c1 = cut(a, Wt, k + 1);
+    if (v > 0 && q.lam <= c0 && c0 < lam_end) scratch[26] = q.ps + tiles_before(q, c0);
+    if (v > 0 && q.lam <= c1 && c1 < lam_end) scratch[27] = q.ps + tiles_before(q, c1);
+    if (threadIdx.x == 0) {  // a cut at the end of the line
+      if (c0 >= Wt) scratch[26] = T;
+      if (c1 >= Wt) scratch[27] = T;
+    }
+    __syncthreads();
+    R0 = scratch[26];
+    R1 = scratch[27];
+    __syncthreads();  // every thread has read R0 and R1
+    if (v > 0 && q.ps <= R0 && R0 < q.ps + v) {
       scratch[1] = s;
-      scratch[2] = excl;
+      scratch[2] = q.ps;
+      scratch[26] = q.lam;  // the first sequence's weighted start (read below)
     }
     __syncthreads();
   } else {  // many sequences: total first, then a chunked scan up to the range start
+    bw = 0;
     long long part = 0;
     for (int s = threadIdx.x; s < S; s += blockDim.x) part += seq_tiles(a, s);
 #pragma unroll
@@ -848,9 +912,12 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     __syncthreads();
     for (int w = 0; w < hpc; ++w) T += scratch[4 + w];
     __syncthreads();
-    const long long r0 = range_start(a, T, k);
+    Wt = static_cast<long long>(kTileWeight) * T;
+    // with no boundary weight the first tile at or after cut(k) is cut(k) / kTileWeight rounded up
+    R0 = (cut(a, Wt, k) + kTileWeight - 1) / kTileWeight;
+    R1 = (cut(a, Wt, k + 1) + kTileWeight - 1) / kTileWeight;
     long long running = 0;
-    for (int base = 0; base < S && running <= r0; base += blockDim.x) {
+    for (int base = 0; base < S && running <= R0; base += blockDim.x) {
       const int s = base + threadIdx.x;
       const long long v = s < S ? seq_tiles(a, s) : 0;
       long long incl = v;
@@ -864,15 +931,15 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
       long long before = running;
       for (int w = 0; w < warp; ++w) before += scratch[4 + w];
       const long long excl = before + incl - v;
-      if (v > 0 && excl <= r0 && r0 < excl + v) {
+      if (v > 0 && excl <= R0 && R0 < excl + v) {
         scratch[1] = s;
         scratch[2] = excl;
+        scratch[26] = kTileWeight * excl;
       }
       for (int w = 0; w < hpc; ++w) running += scratch[4 + w];
       __syncthreads();
     }
   }
-  const long long R0 = range_start(a, T, k), R1 = range_start(a, T, k + 1);
   if (R0 >= R1) return;
   const int n = static_cast<int>(R1 - R0);
   const int s_first = static_cast<int>(scratch[1]);
@@ -885,9 +952,11 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     asm volatile("fence.proxy.async.global;" ::: "memory");
   }
 
+  const long long lam_first = scratch[26];
   if (threadIdx.x == 0) {
-    scratch[0] = T;
+    scratch[0] = Wt;
     scratch[3] = R1;
+    scratch[30] = bw;
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(full_s + 8 * i, 1);
       mbar_init(empty_s + 8 * i, hpc);
@@ -943,6 +1012,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     u.ctx = min(a.context_lens[s_first], a.max_context_len);
     u.tiles = (u.ctx + 15) >> 4;
     u.cls = mixed ? seq_class_of(a, u.s) : 0;
+    u.lam = static_cast<int>(lam_first);
     u.blk = block_of(u);
     if constexpr (split) *cur_blk2 = block2_of(u);
     u.nx_ctx = 0;
@@ -961,6 +1031,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     hd.ps = static_cast<int>(u.ps);
     hd.tiles = u.tiles;
     hd.next_s = u.nx < S ? u.nx : -1;
+    hd.lam = u.lam;
     const int tok = 16 * u.t;
     int blk = u.blk;
     const int cl = mixed ? u.cls : 0;
@@ -1018,6 +1089,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     }
     ++u.i;
     if (++u.t == u.tiles && u.i < n) {  // on to the next sequence with tokens
+      u.lam += kTileWeight * u.tiles + static_cast<int>(scratch[30]);
       u.ps += u.tiles;
       u.t = 0;
       if (u.nx >= S) {  // cannot happen with the tile count T; stay in bounds
@@ -1413,6 +1485,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
         st_relaxed_u64(a.tags + (static_cast<size_t>(k) * HG + hg) * 2 + j, a.epoch);
         scratch[12 + 2 * j] = hd.ps;
         scratch[13 + 2 * j] = (static_cast<long long>(hd.s) << 32) | hd.tiles;
+        scratch[28 + j] = hd.lam;
       }
     }
     __syncwarp();
@@ -1440,31 +1513,30 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     }
     return;
   }
-  const long long Tm = scratch[0];
+  const long long Wm = scratch[0];
+  const int bwm = static_cast<int>(scratch[30]);
   if (warp == pub) {
     __threadfence();
 #pragma unroll 1
     for (int jj = 0; jj < 2; ++jj) {
       const long long info = scratch[13 + 2 * jj];
       if (info < 0) continue;
-      const long long ps = scratch[12 + 2 * jj];
-      const int tiles = static_cast<int>(info & 0xFFFFFFFFll);
-      const int ka = range_of(a, ps, Tm), kb = range_of(a, ps + tiles - 1, Tm);
+      const SeqSpan q{scratch[28 + jj], scratch[12 + 2 * jj],
+                      static_cast<int>(info & 0xFFFFFFFFll), bwm};
+      const int ka = first_range(a, Wm, q), kb = last_range(a, Wm, q);
       const bool tree = kb - ka + 1 > kTreeRanges;
       const int lo = tree ? ka + (k - ka) / kTeam * kTeam : ka;
       const int hi = tree ? min(kb, lo + kTeam - 1) : kb;
       bool done = true;
       for (int kk = lo + lane; kk <= hi; kk += 32) {
-        const long long q0 = range_start(a, Tm, kk), q1 = range_start(a, Tm, kk + 1);
-        if (kk == k || q0 >= q1) continue;  // this range, or an empty one
-        const int j2 = (q0 >= ps) ? 0 : 1;
-        if (ld_relaxed_u64(a.tags + (static_cast<size_t>(kk) * HG + hg) * 2 + j2) != a.epoch)
+        if (kk == k || !holds_tiles(a, Wm, q, kk, kk + 1)) continue;  // this range, or an empty one
+        if (ld_relaxed_u64(a.tags + slot_index(a, Wm, q, kk, HG, hg)) != a.epoch)
           done = false;
       }
       done = __all_sync(0xffffffffu, done);
       if (lane == 0) {  // one merge per sequence (per team)
         unsigned long long* claim =
-            tree ? a.team_claims + slot_index(a, Tm, ps, lo, HG, hg)
+            tree ? a.team_claims + slot_index(a, Wm, q, lo, HG, hg)
                  : a.claims + static_cast<size_t>(info >> 32) * HG + hg;
         if (!done || atomicExch(claim, a.epoch) == a.epoch) scratch[13 + 2 * jj] = -1;
       }
@@ -1477,17 +1549,18 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
   for (int pm = 0; pm < 2; ++pm) {
     const long long info = scratch[13 + 2 * pm];
     if (info < 0) continue;
-    const int s = static_cast<int>(info >> 32), tiles = static_cast<int>(info & 0xFFFFFFFFll);
-    const long long ps = scratch[12 + 2 * pm];
-    const int ka = range_of(a, ps, Tm), kb = range_of(a, ps + tiles - 1, Tm);
+    const int s = static_cast<int>(info >> 32);
+    const SeqSpan q{scratch[28 + pm], scratch[12 + 2 * pm], static_cast<int>(info & 0xFFFFFFFFll),
+                    bwm};
+    const int ka = first_range(a, Wm, q), kb = last_range(a, Wm, q);
     if (kb - ka + 1 <= kTreeRanges) {  // one level: every range's slot, straight to the output
-      merge_slots<D, KVARN>(a, s, ps, Tm, HG, hg, warp, lane, hpc, ka, 1, kb - ka + 1, kb, -1);
+      merge_slots<D, KVARN>(a, s, q, Wm, HG, hg, warp, lane, hpc, ka, 1, kb - ka + 1, kb, -1);
       continue;
     }
     const int nteams = (kb - ka) / kTeam + 1;
     const int lo = ka + (k - ka) / kTeam * kTeam, hi = min(kb, lo + kTeam - 1);
-    const long long rep = slot_index(a, Tm, ps, lo, HG, hg);
-    merge_slots<D, KVARN>(a, s, ps, Tm, HG, hg, warp, lane, hpc, lo, 1, hi - lo + 1, kb, rep);
+    const long long rep = slot_index(a, Wm, q, lo, HG, hg);
+    merge_slots<D, KVARN>(a, s, q, Wm, HG, hg, warp, lane, hpc, lo, 1, hi - lo + 1, kb, rep);
     __syncthreads();  // every warp's rows of the team result are stored
     if (warp == pub) {
       if (lane == 0) {
@@ -1500,10 +1573,8 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
       for (int t = lane; t < nteams; t += 32) {
         const int lo2 = ka + t * kTeam;
         if (lo2 == lo) continue;
-        const long long q0 = range_start(a, Tm, lo2);
-        const long long q1 = range_start(a, Tm, min(lo2 + kTeam, kb + 1));
-        if (q0 >= q1) continue;  // a team of empty ranges
-        if (ld_relaxed_u64(a.team_tags + slot_index(a, Tm, ps, lo2, HG, hg)) != a.epoch)
+        if (!holds_tiles(a, Wm, q, lo2, min(lo2 + kTeam, kb + 1))) continue;  // a team of empty ranges
+        if (ld_relaxed_u64(a.team_tags + slot_index(a, Wm, q, lo2, HG, hg)) != a.epoch)
           done = false;
       }
       done = __all_sync(0xffffffffu, done);
@@ -1515,7 +1586,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     }
     __syncthreads();
     if (scratch[4 + pm])
-      merge_slots<D, KVARN>(a, s, ps, Tm, HG, hg, warp, lane, hpc, ka, kTeam, nteams, kb, -1);
+      merge_slots<D, KVARN>(a, s, q, Wm, HG, hg, warp, lane, hpc, ka, kTeam, nteams, kb, -1);
   }
 }
 
