@@ -487,7 +487,7 @@ __device__ __forceinline__ long long div_floor(long long n, long long d) {
 // a tile belongs to the range whose interval holds its weighted start.  The
 // partition is a fixed function of the lengths and NC.
 constexpr int kTileWeight = 4;
-constexpr int kBoundaryWeight = 6;  // 1.5 tiles: what a boundary costs a range (measured)
+constexpr int kBoundaryWeight = 16;  // 4 tiles: the best of 1.5 to 7 measured on the bench shapes
 
 __device__ __forceinline__ long long cut(const DecodeArgs& a, long long W, int k) {
   return div_floor(W * k, a.num_ctas);
