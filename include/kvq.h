@@ -177,15 +177,18 @@ kvq_status kvq_decode_workspace_size(const kvq_cache_desc* cache, int32_t num_se
  *   the graph starts from clear words (a replay reuses the recorded call's
  *   value).  This holds for kvq_paged_decode(_ex), kvq_decode_append,
  *   kvq_decode_mixed and kvq_paged_decode_static.
- * One kernel launch, stream-K: each CTA owns an equal contiguous range of the
- *   16-token tiles of all sequences (for a group of up to 8 kv-heads).  A
+ * One kernel launch, stream-K: each CTA owns a contiguous range of the 16-token
+ *   tiles of all sequences (for a group of up to 8 kv-heads), the ranges of
+ *   equal weight when each sequence boundary is charged as four tiles.  A
  *   sequence split between CTAs leaves partial results that are merged
  *   (log-sum-exp) by a CTA that, after its own range, finds every other part
  *   published.  Results do not depend on the split beyond rounding.
  * out[s, h] = sum_t softmax_t(sm_scale <q, k_t>) v_t over the dequantized
  *   cache, computed with fp32 softmax and fp32 accumulation (keys and values
  *   enter the tensor cores as exact fp16 code values; the query is rounded to
- *   fp16, which is exact for bf16 values of magnitude 2^-14 .. 65504).
+ *   fp16, which is exact for bf16 values of magnitude 2^-14 .. 65504: smaller
+ *   ones lose bits, larger ones overflow and set KVQ_DEVERR_QUERY_RANGE; the
+ *   16-bit cache keeps the bf16 query).
  */
 kvq_status kvq_paged_decode(const kvq_cache_desc* cache, const void* k_cache,
                             const void* v_cache, void* out, const void* query,
@@ -365,6 +368,10 @@ kvq_status kvq_calibrate_head_scales(const void* x, int64_t num_tokens, int32_t 
 #define KVQ_DEVERR_TIMEOUT 16u      /* a pipeline barrier wait gave up: the CTA stopped
                                        early, the launch's results are invalid */
 #define KVQ_DEVERR_CLASS_RANGE 32u  /* a page class id outside the call's classes */
+#define KVQ_DEVERR_QUERY_RANGE 64u  /* a query value not finite once converted: beyond
+                                       fp16's range (65504) for the quantized formats,
+                                       or an infinity or NaN; that row's output is not
+                                       meaningful */
 
 /*
  * kvq_debug_arm_wait_timeout -- test hook for the decode kernel's bounded

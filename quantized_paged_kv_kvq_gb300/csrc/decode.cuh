@@ -1225,6 +1225,9 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
       }
       __syncwarp();  // every lane has read the rows: fetch the next segment's
       if (hd.next_s >= 0) prefetch_q(hd.next_s);
+      // a query value that is not finite after its conversion (beyond fp16's
+      // range for the quantized formats, or an infinity or NaN in the input)
+      if (__any_sync(0xffffffffu, !isfinite(qs)) && lane == 0) raise_error(64u);  // KVQ_DEVERR_QUERY_RANGE
       qs += __shfl_xor_sync(0xffffffffu, qs, 1);
       qs += __shfl_xor_sync(0xffffffffu, qs, 2);
       qsum0 = __shfl_sync(0xffffffffu, qs, (2 * c) * 4);

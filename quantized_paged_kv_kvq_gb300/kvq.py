@@ -28,6 +28,7 @@ DEVERR_CONTEXT_RANGE = 4
 DEVERR_COMBINE = 8
 DEVERR_TIMEOUT = 16
 DEVERR_CLASS_RANGE = 32
+DEVERR_QUERY_RANGE = 64
 
 
 class KvqError(RuntimeError):

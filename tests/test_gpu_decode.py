@@ -204,3 +204,19 @@ def test_per_head_scales_decode(name, ctas):
     got = out_numpy(g.decode(num_ctas=ctas))
     assert_attention_close(got, OracleRun(wl, head_scales=True).decode(), f"{name} ctas={ctas}")
     assert kvq.kvq_get_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["llama8b_int8", "kvarn_131k", "llama8b_bf16"])
+def test_query_out_of_range_is_flagged(name):
+    """A query value beyond what the decode's query conversion holds (fp16's
+    65504 for the quantized formats; an infinity for the 16-bit cache) sets
+    KVQ_DEVERR_QUERY_RANGE; a query in range sets nothing."""
+    wl = W.workload(name, num_seqs=3, ctx_lo=50, ctx_hi=300)
+    g = GpuRun(wl)
+    g.write()
+    g.decode(num_ctas=2)
+    assert kvq.kvq_get_device_error() == 0
+    big = 1.0e6 if name != "llama8b_bf16" else float("inf")
+    g.query[1, 0, 5] = big
+    g.decode(num_ctas=2)
+    assert kvq.kvq_get_device_error() & kvq.DEVERR_QUERY_RANGE
