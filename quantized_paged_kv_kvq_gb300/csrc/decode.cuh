@@ -822,9 +822,9 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
   // [12..16) partial segments: (first tile, sequence << 32 | tiles) per end of the range,
   // [16..22) producer cursor, [22] second page id, [23] abort flag (int),
   // [24] withheld tile (int; test hook), [25] per end of the range: warps whose
-  // rows of the partial slot are stored (two ints), [26..28) range bounds and the
-  // first sequence's weighted start (prologue), [28..30) per end of the range:
-  // the weighted start of its sequence, [30] the boundary weight
+  // rows of the partial slot are stored (two ints), [26..28) range bounds
+  // (prologue), [28..30) per end of the range: the weighted start of its
+  // sequence, [30] the boundary weight, [31] the first sequence's weighted start
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(scratch + 23);
   int* const done_warps = reinterpret_cast<int*>(scratch + 25);
   const int spin = a.spin_limit;
@@ -836,6 +836,22 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     for (int i = lane; i < G * D / 8; i += 32) cp_async<16>(qbuf_s + 16 * i, src + 8 * i);
     cp_async_commit();
   };
+
+  // ---- the ring's barriers and the CTA's flags (published by the barriers of
+  // the range scan below)
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(full_s + 8 * i, 1);
+      mbar_init(empty_s + 8 * i, hpc);
+    }
+    for (int i = 12; i < 16; ++i) scratch[i] = -1;
+    *abort_flag = 0;
+    reinterpret_cast<int*>(scratch + 24)[0] =
+        (k == a.withhold_cta && hg == 0) ? a.withhold_tile : -1;
+    done_warps[0] = done_warps[1] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
 
   // ---- context checks; zero outputs of the empty sequences this CTA owns
   if (k == 0 && hg == 0) {
@@ -895,11 +911,10 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     __syncthreads();
     R0 = scratch[26];
     R1 = scratch[27];
-    __syncthreads();  // every thread has read R0 and R1
     if (v > 0 && q.ps <= R0 && R0 < q.ps + v) {
       scratch[1] = s;
       scratch[2] = q.ps;
-      scratch[26] = q.lam;  // the first sequence's weighted start (read below)
+      scratch[31] = q.lam;  // the first sequence's weighted start (read below)
     }
     __syncthreads();
   } else {  // many sequences: total first, then a chunked scan up to the range start
@@ -934,7 +949,7 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
       if (v > 0 && excl <= R0 && R0 < excl + v) {
         scratch[1] = s;
         scratch[2] = excl;
-        scratch[26] = kTileWeight * excl;
+        scratch[31] = kTileWeight * excl;
       }
       for (int w = 0; w < hpc; ++w) running += scratch[4 + w];
       __syncthreads();
@@ -952,24 +967,15 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
     asm volatile("fence.proxy.async.global;" ::: "memory");
   }
 
-  const long long lam_first = scratch[26];
-  if (threadIdx.x == 0) {
+  const long long lam_first = scratch[31];
+  if (threadIdx.x == 0) {  // read by thread 0 alone until the barriers after the loop
     scratch[0] = Wt;
     scratch[3] = R1;
     scratch[30] = bw;
-    for (int i = 0; i < C::STAGES; ++i) {
-      mbar_init(full_s + 8 * i, 1);
-      mbar_init(empty_s + 8 * i, hpc);
-    }
-    for (int i = 12; i < 16; ++i) scratch[i] = -1;
-    *abort_flag = 0;
-    reinterpret_cast<int*>(scratch + 24)[0] =
-        (k == a.withhold_cta && hg == 0) ? a.withhold_tile : -1;
-    done_warps[0] = done_warps[1] = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  __syncthreads();
+  // the append's stores before thread 0's first tensor loads (the barriers and
+  // flags were set up before the range scan, whose barriers publish them)
+  if (a.new_key != nullptr) __syncthreads();
 
   // ---- producer cursor (thread 0): walks the range tile by tile
   const uint32_t tile_bytes = hpc * (C::K_HEAD + C::V_HEAD) + hpc * (C::KMF + C::VMF) * 32;
