@@ -70,9 +70,7 @@ __device__ __forceinline__ float tree_sum32(const float (&x)[32]) {
 // of the row (lane bit b set: other - v, else v + other; one fma with a +-1
 // factor is that same single rounding).  Elements 2m and 2m+1 travel as a
 // packed pair, so every stage but h = 1 runs two butterflies per instruction.
-template <int D>
-__device__ __forceinline__ void fwht32(float (&v)[32], int sub) {
-  constexpr int LPR = WideGeom<D>::LPR;
+__device__ __forceinline__ void fwht32_local(float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {  // h = 1: inside a pair
     const float x = v[i], y = v[i + 1];
@@ -90,6 +88,11 @@ __device__ __forceinline__ void fwht32(float (&v)[32], int sub) {
       }
     }
   }
+}
+template <int D>
+__device__ __forceinline__ void fwht32(float (&v)[32], int sub) {
+  constexpr int LPR = WideGeom<D>::LPR;
+  fwht32_local(v);
 #pragma unroll
   for (int lo = 1; lo < LPR; lo <<= 1) {
     const float sgn = (sub & lo) ? -1.0f : 1.0f;
@@ -100,6 +103,49 @@ __device__ __forceinline__ void fwht32(float (&v)[32], int sub) {
       fma2(v[i], v[i + 1], sgn, sgn, v[i], v[i + 1], o0, o1);
     }
   }
+}
+
+// Shared-memory layout of the transpose below (floats): a row's four lanes at
+// kXLane apart, the rows of a warp pass at kXRow apart; with 16-byte accesses
+// both the writes and the transposed reads are free of bank conflicts.
+constexpr int kXLane = 40, kXRow = 164;
+
+// Butterfly stages h = 32 and 64 of a 128-wide row held by four lanes (lane j:
+// elements 32j .. 32j+31) through shared memory: afterwards lane L holds
+// y[8j + t] = element 32j + 8L + t (j < 4, t < 8), so both stages pair values
+// of one lane.  Same pairs, stage order and single roundings as across lanes.
+__device__ __forceinline__ void fwht_cross_transposed(const float (&x)[32], float (&y)[32],
+                                                      float* row_s, int sub) {
+  float* mine = row_s + sub * kXLane;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    *reinterpret_cast<float4*>(mine + 4 * q) =
+        make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float4 f = *reinterpret_cast<const float4*>(row_s + j * kXLane + 8 * sub + 4 * hh);
+      y[8 * j + 4 * hh] = f.x;
+      y[8 * j + 4 * hh + 1] = f.y;
+      y[8 * j + 4 * hh + 2] = f.z;
+      y[8 * j + 4 * hh + 3] = f.w;
+    }
+  __syncwarp();  // the buffer is free for the next row
+#pragma unroll
+  for (int jh = 1; jh <= 2; jh <<= 1)  // h = 32 (j bit 0), then h = 64 (j bit 1)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j & jh) continue;
+#pragma unroll
+      for (int t = 0; t < 8; t += 2) {
+        const int lo = 8 * j + t, hi = 8 * (j + jh) + t;
+        const float a0 = y[lo], a1 = y[lo + 1], b0 = y[hi], b1 = y[hi + 1];
+        add2(y[lo], y[lo + 1], a0, a1, b0, b1);
+        sub2(y[hi], y[hi + 1], a0, a1, b0, b1);
+      }
+    }
 }
 
 // Minimum and maximum of the 32 values (exact): four groups of 8 with
@@ -135,8 +181,11 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
                                                   uint8_t* __restrict__ cache,
                                                   __half* __restrict__ meta, size_t row,
                                                   int64_t blk, int off, int h, int Hkv, int bs,
-                                                  const float2* sgn, float cR) {
+                                                  const float2* sgn, float cR, float* row_s) {
   constexpr int LPR = WideGeom<D>::LPR;
+  // KVarN at D = 128: the last two butterfly stages through shared memory, after
+  // which lane L holds elements 32j + 8L + t (j < 4, t < 8) as x[8j + t]
+  constexpr bool XP = KVARN && D == 128;
   __half sig16 = __float2half_rn(1.0f);
   if constexpr (KVARN) {
     const float inv_d = 1.0f / D;  // exact (power of two)
@@ -163,7 +212,15 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
       mul2(x[i], x[i + 1], x[i], x[i + 1], m0, m1);
       mul2(x[i + 2], x[i + 3], x[i + 2], x[i + 3], m2, m3);
     }
-    fwht32<D>(x, sub);
+    if constexpr (XP) {
+      fwht32_local(x);
+      float y[32];
+      fwht_cross_transposed(x, y, row_s, sub);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = y[i];
+    } else {
+      fwht32<D>(x, sub);
+    }
 #pragma unroll
     for (int i = 0; i < 32; i += 2) mul2(x[i], x[i + 1], x[i], x[i + 1], cR, cR);
   }
@@ -204,9 +261,16 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
       code2(8 * k, c0, c1);
       ww[k] = pack_sat_u4(c1, c0, t);
     }
-    if (active)
-      *reinterpret_cast<uint4*>(cache + row * (D / 2) + sub * 16) =
-          make_uint4(ww[0], ww[1], ww[2], ww[3]);
+    if (active) {
+      if constexpr (XP) {  // word j: elements 32j + 8 sub .. + 7
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint32_t*>(cache + row * (D / 2) + 16 * j + 4 * sub) = ww[j];
+      } else {
+        *reinterpret_cast<uint4*>(cache + row * (D / 2) + sub * 16) =
+            make_uint4(ww[0], ww[1], ww[2], ww[3]);
+      }
+    }
   } else {  // element i in byte i
     uint32_t ww[8];
 #pragma unroll
@@ -217,9 +281,16 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
       ww[k] = pack_sat_u8(c1, c0, pack_sat_u8(c3, c2, 0u));
     }
     if (active) {
-      uint4* dst = reinterpret_cast<uint4*>(cache + row * D + sub * 32);
-      dst[0] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
-      dst[1] = make_uint4(ww[4], ww[5], ww[6], ww[7]);
+      if constexpr (XP) {  // words 2j, 2j+1: elements 32j + 8 sub .. + 7
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint2*>(cache + row * D + 32 * j + 8 * sub) =
+              make_uint2(ww[2 * j], ww[2 * j + 1]);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(cache + row * D + sub * 32);
+        dst[0] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+        dst[1] = make_uint4(ww[4], ww[5], ww[6], ww[7]);
+      }
     }
   }
   if (active) {
@@ -240,23 +311,24 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
 template <int D, int KF, int VF, bool KVARN, class Reload>
 __device__ __forceinline__ void quantize_pass(float (&x)[32], const Reload& reload,
                                               const WriteArgs& a, int r, int sub, size_t row0,
-                                              long long blk, int off, const float2* lane_sgn) {
+                                              long long blk, int off, const float2* lane_sgn,
+                                              float* row_s) {
   const int Hkv = a.num_kv_heads;
   const bool act = r < 2 * Hkv;
   const bool is_v = r >= Hkv;
   const int h = is_v ? r - Hkv : r;
   if (__all_sync(0xffffffffu, !is_v || !act)) {
     quantize_row_wide<D, KF, KVARN>(x, sub, act, a.k_cache, a.k_meta, row0 + h, blk, off, h, Hkv,
-                                    a.block_size, lane_sgn, a.cR);
+                                    a.block_size, lane_sgn, a.cR, row_s);
   } else if (__all_sync(0xffffffffu, is_v || !act)) {
     quantize_row_wide<D, VF, KVARN>(x, sub, act, a.v_cache, a.v_meta, row0 + h, blk, off, h, Hkv,
-                                    a.block_size, lane_sgn, a.cR);
+                                    a.block_size, lane_sgn, a.cR, row_s);
   } else {  // a pass with K and V rows (fewer kv-heads than rows per pass)
     quantize_row_wide<D, KF, KVARN>(x, sub, act && !is_v, a.k_cache, a.k_meta, row0 + h, blk, off,
-                                    h, Hkv, a.block_size, lane_sgn, a.cR);
+                                    h, Hkv, a.block_size, lane_sgn, a.cR, row_s);
     if constexpr (KVARN) reload(x);  // the K rows were rotated in place
     quantize_row_wide<D, VF, KVARN>(x, sub, act && is_v, a.v_cache, a.v_meta, row0 + h, blk, off,
-                                    h, Hkv, a.block_size, lane_sgn, a.cR);
+                                    h, Hkv, a.block_size, lane_sgn, a.cR, row_s);
   }
 }
 
@@ -286,9 +358,12 @@ __global__ void __launch_bounds__(kWriteWarps * 32, ctas_per_sm(KVARN))
     write_asym_kernel(WriteArgs a) {
   constexpr int LPR = WideGeom<D>::LPR, RPW = WideGeom<D>::RPW;
   __shared__ __align__(16) float2 sgn[KVARN ? D / 2 : 1];
+  // the transpose of the last butterfly stages (KVarN, D = 128): a slot per row of a pass
+  __shared__ __align__(16) float xpose[KVARN && D == 128 ? kWriteWarps * RPW * kXRow : 4];
   fill_sign_pairs<D, KVARN>(sgn, a.signs);
   const int lane = threadIdx.x & 31;
   const int sub = lane % LPR, grp = lane / LPR;
+  float* const row_s = KVARN && D == 128 ? xpose + ((threadIdx.x >> 5) * RPW + grp) * kXRow : nullptr;
   const int Hkv = a.num_kv_heads;
   const float2* lane_sgn = sgn + (KVARN ? sign_pair_index<D>(sub * 16) : 0);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kWriteWarps;
@@ -322,7 +397,7 @@ __global__ void __launch_bounds__(kWriteWarps * 32, ctas_per_sm(KVARN))
       };
       float x[32];
       load(x);
-      quantize_pass<D, KF, VF, KVARN>(x, load, a, r, sub, row0, blk, off, lane_sgn);
+      quantize_pass<D, KF, VF, KVARN>(x, load, a, r, sub, row0, blk, off, lane_sgn, row_s);
     }
   }
 }
