@@ -200,8 +200,7 @@ kvq_status kvq_paged_decode(const kvq_cache_desc* cache, const void* k_cache,
 /*
  * kvq_paged_decode_ex -- kvq_paged_decode with an explicit number of CTAs
  * per group of 8 kv-heads (the stream-K ranges the tiles are split into,
- * 1..65535; 0 = the automatic choice: two per SM, one for the 16-bit cache and
- * for KVarN).  The workspace must hold
+ * 1..65535; 0 = the automatic choice: two per SM, one for the 16-bit cache).  The workspace must hold
  * kvq_decode_workspace_size_ex(...) bytes for the same num_ctas.
  */
 kvq_status kvq_decode_workspace_size_ex(const kvq_cache_desc* cache, int32_t num_seqs,

@@ -83,8 +83,7 @@ int heads_per_cta(int hkv) { return hkv < 8 ? hkv : 8; }
 
 // Stream-K ranges per head group: as many as the decode kernel has resident
 // CTAs (two per SM; one for the 16-bit cache, whose 64 KB stages fill an
-// SM's shared memory, and one for KVarN, whose rotation and three metadata
-// fields spill at the two-CTA register budget), at most one per possible tile.
+// SM's shared memory), at most one per possible tile.
 int auto_ctas(int num_seqs, int max_ctx, int head_groups, int sms, int per_sm) {
   const long long tiles_max = static_cast<long long>(num_seqs) * ((max_ctx + 15) / 16);
   long long nc =
@@ -145,7 +144,7 @@ kvq_status decode_shape(const kvq_cache_desc* c, int32_t num_seqs, int32_t num_q
     const int sms = sm_count();
     if (sms <= 0) return KVQ_ERR_CUDA;
     nc = auto_ctas(num_seqs, max_context_len, c->num_kv_heads / heads_per_cta(c->num_kv_heads),
-                   sms, (c->k_fmt == KVQ_FMT_BF16 || (c->flags & KVQ_FLAG_VARNORM_ROTATE)) ? 1 : 2);
+                   sms, c->k_fmt == KVQ_FMT_BF16 ? 1 : 2);
   }
   *NC = nc;
   return KVQ_OK;

@@ -78,9 +78,8 @@ struct DecodeCfg {
     return align(hpc * K_HEAD) + align(hpc * V_HEAD) + align(meta_room(hpc, KMF) + meta_room(hpc, VMF));
   }
   static constexpr int STAGE_MAX = stage_bytes(kHeadsPerCta);
-  // ring depth: about 96 KB of tiles per CTA with two CTAs per SM; KVarN runs
-  // one CTA per SM (its registers) with six stages
-  static constexpr int STAGES = KVARN ? 6 : STAGE_MAX >= 24576 ? 3 : STAGE_MAX >= 16384 ? 5 : 6;
+  // ring depth: about 96 KB of tiles per CTA with two CTAs per SM
+  static constexpr int STAGES = STAGE_MAX >= 24576 ? 3 : STAGE_MAX >= 16384 ? 5 : 6;
   static constexpr int EB = KF == BF16 ? 2 : 1;  // K element bytes (INT4: see kslot_d)
   static constexpr bool KVARN_ = KVARN;
   static_assert(KW * 4 == K_LANE && VW * 4 == VPS, "layout");
@@ -459,6 +458,9 @@ __device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
   return r;
 }
+__device__ __forceinline__ void sts_u16(uint32_t a, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
+}
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -782,10 +784,9 @@ __device__ __forceinline__ void append_new_tokens(const DecodeArgs& a, long long
 // page class); separate instances, so that one page size keeps the one-box
 // path's registers.
 // Two CTAs per SM (128 registers a thread), except the 16-bit cache (its
-// stages fill shared memory) and KVarN (the rotation and its metadata need
-// more registers): one.
+// stages fill shared memory): one.
 template <int D, int KF, int VF, bool KVARN, int PAGES>
-__global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 : 2)
+__global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16) ? 1 : 2)
     decode_partition_kernel(const DecodeArgs a, const __grid_constant__ DecodeMapsOf<PAGES> maps) {
   using C = DecodeCfg<D, KF, VF, KVARN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1183,51 +1184,40 @@ __global__ void __launch_bounds__(kHeadsPerCta * 32, (KF == BF16 || KVARN) ? 1 :
       __syncwarp();
       float qs = 0.0f, qh = 0.0f;  // qh: the k-slots that meet high nibbles (int4 K)
       if constexpr (KVARN) {
+        // each query row of the group is rotated in a float row and written back
+        // over its bf16 row as fp16 (the rounding every quantized format gives
+        // the query), so the fragments below read it like any other row
         float* srow = reinterpret_cast<float*>(smem + rot_off + warp * D * 4);
-        float qv[C::KSTEPS][4];
         for (int nn = 0; nn < G; ++nn) {
           for (int e = lane; e < D; e += 32)
             srow[e] = __uint_as_float(static_cast<uint32_t>(lds_u16(qbuf_s + 2 * (nn * D + e))) << 16);
           __syncwarp();
           rotate_row_warp<D, false>(srow, a.signs, a.cR, lane);
-          if (g == nn) {
-#pragma unroll
-            for (int j = 0; j < C::KSTEPS; ++j)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) qv[j][e] = srow[kslot_d<D, KF>(c, j, e)];
-          }
+          for (int e = lane; e < D; e += 32)
+            sts_u16(qbuf_s + 2 * (nn * D + e), __half_as_ushort(__float2half_rn(srow[e])));
           __syncwarp();
         }
+      }
 #pragma unroll
-        for (int j = 0; j < C::KSTEPS; ++j) {
-          float v[4];
+      for (int j = 0; j < C::KSTEPS; ++j) {
+        float v[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v[e] = g < G ? __half2float(__float2half_rn(qv[j][e])) : 0.0f;
-            qs += v[e];
-            if (e >= 2) qh += v[e];
-          }
-          qf[j][0] = pack_half2(v[0], v[1]);
-          qf[j][1] = pack_half2(v[2], v[3]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < C::KSTEPS; ++j) {
-          float v[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v[e] = 0.0f;
-            if (g < G) {
-              v[e] = __uint_as_float(
-                  static_cast<uint32_t>(lds_u16(qbuf_s + 2 * (g * D + kslot_d<D, KF>(c, j, e)))) << 16);
+        for (int e = 0; e < 4; ++e) {
+          v[e] = 0.0f;
+          if (g < G) {
+            const uint16_t bits = lds_u16(qbuf_s + 2 * (g * D + kslot_d<D, KF>(c, j, e)));
+            if constexpr (KVARN) {
+              v[e] = __half2float(__ushort_as_half(bits));
+            } else {
+              v[e] = __uint_as_float(static_cast<uint32_t>(bits) << 16);
               if constexpr (KF != BF16) v[e] = __half2float(__float2half_rn(v[e]));
             }
-            qs += v[e];
-            if (e >= 2) qh += v[e];
           }
-          qf[j][0] = pack_op2<KF == BF16>(v[0], v[1]);  // exact (bf16 or its fp16 rounding)
-          qf[j][1] = pack_op2<KF == BF16>(v[2], v[3]);
+          qs += v[e];
+          if (e >= 2) qh += v[e];
         }
+        qf[j][0] = pack_op2<KF == BF16>(v[0], v[1]);  // exact (bf16 or its fp16 rounding)
+        qf[j][1] = pack_op2<KF == BF16>(v[2], v[3]);
       }
       __syncwarp();  // every lane has read the rows: fetch the next segment's
       if (hd.next_s >= 0) prefetch_q(hd.next_s);

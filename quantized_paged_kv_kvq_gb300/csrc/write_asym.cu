@@ -188,6 +188,11 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
   constexpr bool XP = KVARN && D == 128;
   __half sig16 = __float2half_rn(1.0f);
   if constexpr (KVARN) {
+    // Every packed product below feeds a scalar add (the sum tree, the h = 1
+    // butterfly) or no add at all: ptxas contracts a packed multiply and a
+    // packed add of the same pairs into one FFMA2 even with .rn, which would
+    // skip the product's rounding (seen on the squared deviations when the
+    // tree ran on packed pairs).
     const float inv_d = 1.0f / D;  // exact (power of two)
     const float mean = __fmul_rn(tree_sum32<D>(x), inv_d);
     float sq[32];

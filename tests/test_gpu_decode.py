@@ -119,6 +119,7 @@ SMALL_PAGE_SHAPES = {
     "int8_d64_2heads": ("tiny_int8", {}),
     "int4_d64_2heads": ("llama70b_int4", dict(num_q_heads=8, num_kv_heads=2, head_dim=64)),
     "kvarn_d128_2heads": ("kvarn_131k", dict(num_q_heads=8, num_kv_heads=2)),
+    "kvarn_d64_2heads": ("kvarn_131k", dict(num_q_heads=8, num_kv_heads=2, head_dim=64)),
     "fp8_d128_4heads": ("llama8b_e4m3k_int8v", dict(num_q_heads=16, num_kv_heads=4)),
     "bf16_d128_2heads": ("llama8b_bf16", dict(num_q_heads=8, num_kv_heads=2)),
     "bf16_d64_2heads": ("llama8b_bf16", dict(num_q_heads=8, num_kv_heads=2, head_dim=64)),
