@@ -39,6 +39,30 @@ def test_write_bitexact_small(name):
     assert kvq.kvq_get_device_error() == 0
 
 
+# More kv-heads than one warp pass holds: a token's rows take several passes,
+# which the write spreads over different warps (head_dim 128: 8 rows a pass, so
+# 24 rows are three passes; head_dim 64: 16 rows a pass, so the first pass
+# holds K and V rows and the second is partly empty).
+MANY_HEADS = {
+    "kvarn_d128_12heads": ("kvarn_131k", dict(num_q_heads=12, num_kv_heads=12)),
+    "kvarn_d64_12heads": ("kvarn_131k", dict(num_q_heads=12, num_kv_heads=12, head_dim=64)),
+    "int4_d128_12heads": ("llama70b_int4", dict(num_q_heads=12, num_kv_heads=12)),
+}
+
+
+@pytest.mark.parametrize("shape", list(MANY_HEADS))
+def test_write_bitexact_many_heads(shape):
+    name, kw = MANY_HEADS[shape]
+    wl = W.workload(name, **dict(kw, num_seqs=3, ctx_lo=1, ctx_hi=300))
+    g = GpuRun(wl)
+    o = OracleRun(wl)
+    g.write()
+    kc, km, vc, vm = g.cache_numpy()
+    assert np.array_equal(kc, o.kc) and np.array_equal(vc, o.vc), f"{shape}: codes"
+    assert np.array_equal(km, o.km) and np.array_equal(vm, o.vm), f"{shape}: meta"
+    assert kvq.kvq_get_device_error() == 0
+
+
 def _all_bf16_finite():
     bits = np.arange(1 << 16, dtype=np.uint32) << 16
     x = bits.view(np.float32)
