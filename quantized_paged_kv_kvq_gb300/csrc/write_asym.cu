@@ -39,13 +39,15 @@ template <int D>
 struct WideGeom {
   static constexpr int LPR = D / 32;    // lanes per row
   static constexpr int RPW = 32 / LPR;  // rows per warp pass
-  static constexpr int GPL = 4;         // groups of 8 per lane
 };
 
 // Fixed-order float32 sum of a row: each group of 8 left to right, then every
 // group sum s_j becomes s_j + s_(j xor o) for o = D/16, ..., 1 (group j of the
-// row is group j % 4 of lane j / 4 of the row's lanes).
-template <int D>
+// row is group j % 4 of lane j / 4 of the row's lanes).  XP: the lane's blocks
+// are permuted (register block b of lane L is the lane's block b xor L, see
+// bfly_blocks), so the partner lane's group sits in register block b xor o;
+// each add is commutative, so every lane still forms the same sums.
+template <int D, bool XP>
 __device__ __forceinline__ float tree_sum32(const float (&x)[32]) {
   constexpr int LPR = WideGeom<D>::LPR;
   float g[4];
@@ -59,26 +61,50 @@ __device__ __forceinline__ float tree_sum32(const float (&x)[32]) {
   // offsets D/16 .. 4 cross lanes (lane offset o / 4), then 2 and 1 are local
 #pragma unroll
   for (int lo = LPR / 2; lo >= 1; lo >>= 1) {
+    float o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) g[j] = __fadd_rn(g[j], __shfl_xor_sync(0xffffffffu, g[j], lo));
+    for (int j = 0; j < 4; ++j) o[j] = __shfl_xor_sync(0xffffffffu, g[XP ? (j ^ lo) : j], lo);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) g[j] = __fadd_rn(g[j], o[j]);
   }
   const float a0 = __fadd_rn(g[0], g[2]), a1 = __fadd_rn(g[1], g[3]);
   return __fadd_rn(a0, a1);
+}
+
+// A butterfly stage between register blocks b and b + hb/8 (hb = 8 or 16) whose
+// roles depend on the lane: s = +1 when the lower register block holds the
+// lower element of each pair, -1 when it holds the upper one.  Then
+// lower + upper = s*v[lo] + v[hi] lands in the slot of the lower element and
+// lower - upper in the other (-s*v[hi] + v[lo]); an fma with a +-1 factor is
+// the single rounding of that sum or difference.
+__device__ __forceinline__ void bfly_blocks(float (&v)[32], int hb, float s) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    if ((i & hb) == 0) {
+      const float a0 = v[i], a1 = v[i + 1], b0 = v[i + hb], b1 = v[i + hb + 1];
+      fma2(v[i], v[i + 1], s, s, a0, a1, b0, b1);
+      fma2(v[i + hb], v[i + hb + 1], -s, -s, b0, b1, a0, a1);
+    }
+  }
 }
 
 // Butterfly stages h = 1 .. 16 in registers, then h = 32, 64 across the lanes
 // of the row (lane bit b set: other - v, else v + other; one fma with a +-1
 // factor is that same single rounding).  Elements 2m and 2m+1 travel as a
 // packed pair, so every stage but h = 1 runs two butterflies per instruction.
-__device__ __forceinline__ void fwht32_local(float (&v)[32]) {
+// XP (KVarN, D = 128): register block b of lane L holds the lane's block b xor
+// L, so stages h = 8, 16 pair register blocks with lane-dependent roles.
+template <bool XP>
+__device__ __forceinline__ void fwht32_local(float (&v)[32], int sub) {
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {  // h = 1: inside a pair
     const float x = v[i], y = v[i + 1];
     v[i] = __fadd_rn(x, y);
     v[i + 1] = __fsub_rn(x, y);
   }
+  // h = 2, 4 inside the 8-element blocks; h = 8, 16 between them
 #pragma unroll
-  for (int h = 2; h < 32; h <<= 1) {
+  for (int h = 2; h < (XP ? 8 : 32); h <<= 1) {
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
       if ((i & h) == 0) {
@@ -88,11 +114,15 @@ __device__ __forceinline__ void fwht32_local(float (&v)[32]) {
       }
     }
   }
+  if constexpr (XP) {
+    bfly_blocks(v, 8, (sub & 1) ? -1.0f : 1.0f);
+    bfly_blocks(v, 16, (sub & 2) ? -1.0f : 1.0f);
+  }
 }
 template <int D>
 __device__ __forceinline__ void fwht32(float (&v)[32], int sub) {
   constexpr int LPR = WideGeom<D>::LPR;
-  fwht32_local(v);
+  fwht32_local<false>(v, sub);
 #pragma unroll
   for (int lo = 1; lo < LPR; lo <<= 1) {
     const float sgn = (sub & lo) ? -1.0f : 1.0f;
@@ -105,47 +135,20 @@ __device__ __forceinline__ void fwht32(float (&v)[32], int sub) {
   }
 }
 
-// Shared-memory layout of the transpose below (floats): a row's four lanes at
-// kXLane apart, the rows of a warp pass at kXRow apart; with 16-byte accesses
-// both the writes and the transposed reads are free of bank conflicts.
-constexpr int kXLane = 40, kXRow = 164;
-
-// Butterfly stages h = 32 and 64 of a 128-wide row held by four lanes (lane j:
-// elements 32j .. 32j+31) through shared memory: afterwards lane L holds
-// y[8j + t] = element 32j + 8L + t (j < 4, t < 8), so both stages pair values
-// of one lane.  Same pairs, stage order and single roundings as across lanes.
-__device__ __forceinline__ void fwht_cross_transposed(const float (&x)[32], float (&y)[32],
-                                                      float* row_s, int sub) {
-  float* mine = row_s + sub * kXLane;
+// Butterfly stages h = 32 and 64 of a 128-wide row held by four lanes in the
+// XP layout (register block b of lane L = elements 32L + 8(b xor L) .. + 7):
+// register block b (b = 1, 2, 3) of every lane goes to lane L xor b, whose
+// block it is, and block 0 stays.  Afterwards register block b of lane L holds
+// elements 32(L xor b) + 8L .. + 7, so both stages pair register blocks, with
+// the roles of the local ones.  Same pairs, stage order and single roundings
+// as across lanes; 24 shuffles.
+__device__ __forceinline__ void fwht_cross_xor(float (&v)[32], int sub) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q)
-    *reinterpret_cast<float4*>(mine + 4 * q) =
-        make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-  __syncwarp();
+  for (int bb = 1; bb < 4; ++bb)
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const float4 f = *reinterpret_cast<const float4*>(row_s + j * kXLane + 8 * sub + 4 * hh);
-      y[8 * j + 4 * hh] = f.x;
-      y[8 * j + 4 * hh + 1] = f.y;
-      y[8 * j + 4 * hh + 2] = f.z;
-      y[8 * j + 4 * hh + 3] = f.w;
-    }
-  __syncwarp();  // the buffer is free for the next row
-#pragma unroll
-  for (int jh = 1; jh <= 2; jh <<= 1)  // h = 32 (j bit 0), then h = 64 (j bit 1)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (j & jh) continue;
-#pragma unroll
-      for (int t = 0; t < 8; t += 2) {
-        const int lo = 8 * j + t, hi = 8 * (j + jh) + t;
-        const float a0 = y[lo], a1 = y[lo + 1], b0 = y[hi], b1 = y[hi + 1];
-        add2(y[lo], y[lo + 1], a0, a1, b0, b1);
-        sub2(y[hi], y[hi + 1], a0, a1, b0, b1);
-      }
-    }
+    for (int t = 0; t < 8; ++t) v[8 * bb + t] = __shfl_xor_sync(0xffffffffu, v[8 * bb + t], bb);
+  bfly_blocks(v, 8, (sub & 1) ? -1.0f : 1.0f);   // h = 32
+  bfly_blocks(v, 16, (sub & 2) ? -1.0f : 1.0f);  // h = 64
 }
 
 // Minimum and maximum of the 32 values (exact): four groups of 8 with
@@ -181,10 +184,12 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
                                                   uint8_t* __restrict__ cache,
                                                   __half* __restrict__ meta, size_t row,
                                                   int64_t blk, int off, int h, int Hkv, int bs,
-                                                  const float2* sgn, float cR, float* row_s) {
+                                                  const float2* sgn, float cR) {
   constexpr int LPR = WideGeom<D>::LPR;
-  // KVarN at D = 128: the last two butterfly stages through shared memory, after
-  // which lane L holds elements 32j + 8L + t (j < 4, t < 8) as x[8j + t]
+  // KVarN at D = 128: the lane's blocks arrive permuted (register block b of
+  // lane L = its block b xor L) and the last two butterfly stages exchange
+  // blocks by shuffles, after which register block b of lane L holds elements
+  // 32(L xor b) + 8L + t (t < 8)
   constexpr bool XP = KVARN && D == 128;
   __half sig16 = __float2half_rn(1.0f);
   if constexpr (KVARN) {
@@ -194,7 +199,7 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
     // skip the product's rounding (seen on the squared deviations when the
     // tree ran on packed pairs).
     const float inv_d = 1.0f / D;  // exact (power of two)
-    const float mean = __fmul_rn(tree_sum32<D>(x), inv_d);
+    const float mean = __fmul_rn(tree_sum32<D, XP>(x), inv_d);
     float sq[32];
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
@@ -202,7 +207,7 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
       sub2(d0, d1, x[i], x[i + 1], mean, mean);
       mul2(sq[i], sq[i + 1], d0, d1, d0, d1);
     }
-    const float var = __fmul_rn(tree_sum32<D>(sq), inv_d);
+    const float var = __fmul_rn(tree_sum32<D, XP>(sq), inv_d);
     sig16 = __float2half_rn(__fsqrt_rn(var));
     if (__half2float(sig16) == 0.0f) sig16 = __float2half_rn(1.0f);
     const float inv_sigma = __frcp_rn(__half2float(sig16));
@@ -218,11 +223,8 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
       mul2(x[i + 2], x[i + 3], x[i + 2], x[i + 3], m2, m3);
     }
     if constexpr (XP) {
-      fwht32_local(x);
-      float y[32];
-      fwht_cross_transposed(x, y, row_s, sub);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = y[i];
+      fwht32_local<true>(x, sub);
+      fwht_cross_xor(x, sub);
     } else {
       fwht32<D>(x, sub);
     }
@@ -267,10 +269,10 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
       ww[k] = pack_sat_u4(c1, c0, t);
     }
     if (active) {
-      if constexpr (XP) {  // word j: elements 32j + 8 sub .. + 7
+      if constexpr (XP) {  // word b: elements 32(b xor sub) + 8 sub .. + 7
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint32_t*>(cache + row * (D / 2) + 16 * j + 4 * sub) = ww[j];
+        for (int b = 0; b < 4; ++b)
+          *reinterpret_cast<uint32_t*>(cache + row * (D / 2) + 16 * (b ^ sub) + 4 * sub) = ww[b];
       } else {
         *reinterpret_cast<uint4*>(cache + row * (D / 2) + sub * 16) =
             make_uint4(ww[0], ww[1], ww[2], ww[3]);
@@ -286,11 +288,11 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
       ww[k] = pack_sat_u8(c1, c0, pack_sat_u8(c3, c2, 0u));
     }
     if (active) {
-      if constexpr (XP) {  // words 2j, 2j+1: elements 32j + 8 sub .. + 7
+      if constexpr (XP) {  // words 2b, 2b+1: elements 32(b xor sub) + 8 sub .. + 7
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint2*>(cache + row * D + 32 * j + 8 * sub) =
-              make_uint2(ww[2 * j], ww[2 * j + 1]);
+        for (int b = 0; b < 4; ++b)
+          *reinterpret_cast<uint2*>(cache + row * D + 32 * (b ^ sub) + 8 * sub) =
+              make_uint2(ww[2 * b], ww[2 * b + 1]);
       } else {
         uint4* dst = reinterpret_cast<uint4*>(cache + row * D + sub * 32);
         dst[0] = make_uint4(ww[0], ww[1], ww[2], ww[3]);
@@ -316,36 +318,40 @@ __device__ __forceinline__ void quantize_row_wide(float (&x)[32], int sub, bool 
 template <int D, int KF, int VF, bool KVARN, class Reload>
 __device__ __forceinline__ void quantize_pass(float (&x)[32], const Reload& reload,
                                               const WriteArgs& a, int r, int sub, size_t row0,
-                                              long long blk, int off, const float2* lane_sgn,
-                                              float* row_s) {
+                                              long long blk, int off, const float2* lane_sgn) {
   const int Hkv = a.num_kv_heads;
   const bool act = r < 2 * Hkv;
   const bool is_v = r >= Hkv;
   const int h = is_v ? r - Hkv : r;
   if (__all_sync(0xffffffffu, !is_v || !act)) {
     quantize_row_wide<D, KF, KVARN>(x, sub, act, a.k_cache, a.k_meta, row0 + h, blk, off, h, Hkv,
-                                    a.block_size, lane_sgn, a.cR, row_s);
+                                    a.block_size, lane_sgn, a.cR);
   } else if (__all_sync(0xffffffffu, is_v || !act)) {
     quantize_row_wide<D, VF, KVARN>(x, sub, act, a.v_cache, a.v_meta, row0 + h, blk, off, h, Hkv,
-                                    a.block_size, lane_sgn, a.cR, row_s);
+                                    a.block_size, lane_sgn, a.cR);
   } else {  // a pass with K and V rows (fewer kv-heads than rows per pass)
     quantize_row_wide<D, KF, KVARN>(x, sub, act && !is_v, a.k_cache, a.k_meta, row0 + h, blk, off,
-                                    h, Hkv, a.block_size, lane_sgn, a.cR, row_s);
+                                    h, Hkv, a.block_size, lane_sgn, a.cR);
     if constexpr (KVARN) reload(x);  // the K rows were rotated in place
     quantize_row_wide<D, VF, KVARN>(x, sub, act && is_v, a.v_cache, a.v_meta, row0 + h, blk, off,
-                                    h, Hkv, a.block_size, lane_sgn, a.cR, row_s);
+                                    h, Hkv, a.block_size, lane_sgn, a.cR);
   }
 }
 
-// The rotation's diagonal as +-1.0f pairs in shared memory (sign_pair_index).
+// The rotation's diagonal as +-1.0f pairs in shared memory (sign_pair_index),
+// in the order of each lane's registers: pair ml of lane sub (m = 16 sub + ml)
+// holds the signs of the elements in its registers 2 ml, 2 ml + 1, which at
+// D = 128 are the lane's block (ml / 4) xor sub, offset 2 (ml % 4).
 template <int D, bool KVARN>
 __device__ __forceinline__ void fill_sign_pairs(float2* sgn, const int8_t* signs) {
   if constexpr (KVARN) {
     for (int m = threadIdx.x; m < D / 2; m += blockDim.x) {
+      const int sub = m / 16, ml = m % 16;
+      const int mg = D == 128 ? 16 * sub + 4 * ((ml / 4) ^ sub) + ml % 4 : m;
       float2 p = make_float2(1.0f, 1.0f);
       if (signs != nullptr) {
-        p.x = signs[2 * m] < 0 ? -1.0f : 1.0f;
-        p.y = signs[2 * m + 1] < 0 ? -1.0f : 1.0f;
+        p.x = signs[2 * mg] < 0 ? -1.0f : 1.0f;
+        p.y = signs[2 * mg + 1] < 0 ? -1.0f : 1.0f;
       }
       sgn[sign_pair_index<D>(m)] = p;
     }
@@ -363,12 +369,9 @@ __global__ void __launch_bounds__(kWriteWarps * 32, ctas_per_sm(KVARN))
     write_asym_kernel(WriteArgs a) {
   constexpr int LPR = WideGeom<D>::LPR, RPW = WideGeom<D>::RPW;
   __shared__ __align__(16) float2 sgn[KVARN ? D / 2 : 1];
-  // the transpose of the last butterfly stages (KVarN, D = 128): a slot per row of a pass
-  __shared__ __align__(16) float xpose[KVARN && D == 128 ? kWriteWarps * RPW * kXRow : 4];
   fill_sign_pairs<D, KVARN>(sgn, a.signs);
   const int lane = threadIdx.x & 31;
   const int sub = lane % LPR, grp = lane / LPR;
-  float* const row_s = KVARN && D == 128 ? xpose + ((threadIdx.x >> 5) * RPW + grp) * kXRow : nullptr;
   const int Hkv = a.num_kv_heads;
   const float2* lane_sgn = sgn + (KVARN ? sign_pair_index<D>(sub * 16) : 0);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kWriteWarps;
@@ -395,14 +398,16 @@ __global__ void __launch_bounds__(kWriteWarps * 32, ctas_per_sm(KVARN))
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float e[8];
-          unpack8(act ? ldg_stream16(src + 8 * q) : make_uint4(0, 0, 0, 0), e);
+          // KVarN at D = 128: register block q holds the lane's block q xor sub
+          const int qb = (KVARN && D == 128) ? (q ^ sub) : q;
+          unpack8(act ? ldg_stream16(src + 8 * qb) : make_uint4(0, 0, 0, 0), e);
 #pragma unroll
           for (int i = 0; i < 8; ++i) y[8 * q + i] = e[i];
         }
       };
       float x[32];
       load(x);
-      quantize_pass<D, KF, VF, KVARN>(x, load, a, r, sub, row0, blk, off, lane_sgn, row_s);
+      quantize_pass<D, KF, VF, KVARN>(x, load, a, r, sub, row0, blk, off, lane_sgn);
     }
   }
 }
